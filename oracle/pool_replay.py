@@ -1,0 +1,141 @@
+"""Block bookkeeping of the paged KV cache, replayed in plain Python.
+
+TEST INFRASTRUCTURE ONLY (part of the oracle).  It is written independently
+of the library's C++ block pool and is compared with it step by step.
+
+Rules, in the pages' terms:
+
+* A request's KV cache is a list of logical blocks filled left to right; a
+  block table maps each logical block to a physical block.  A new physical
+  block is taken only when the last one is full, so all waste sits in the last
+  block (studying-code.tistory.com/16, sections "vLLM의 메모리 관리" and
+  "물리적 블록 할당"; tech.blogsailing.com/?p=100 section 2, ``append_token``:
+  logical block = token_idx // BLOCK_SIZE, offset = token_idx % BLOCK_SIZE,
+  a new block is popped from the front of the free pool only when the logical
+  block does not exist yet).
+* A prompt of n tokens takes ceil(n / block_size) blocks
+  (itan.pw "vLLMにおけるKVCacheマネージャーの詳細解説", section
+  "ブロック割当のロジック": cdiv(num_tokens, block_size)).
+* Forking a sequence shares all its physical blocks and raises each block's
+  reference count (studying-code.tistory.com/16, the two-sample example before
+  "생성 단계에서의 Copy-on-Write"; tech.blogsailing.com/?p=100 section 3,
+  ``fork_sequence``).
+* Copy-on-write: a sequence about to write into a block whose reference count
+  is above 1 takes a new block, the old block's content is copied to it, and
+  the old block's count drops by one; a holder that finds the count at 1
+  writes in place (studying-code.tistory.com/16, section "생성 단계에서의
+  Copy-on-Write"; tech.blogsailing.com/?p=100 section 3, ``resolve_cow``).
+  The copy is reported as a (src, dst) pair for the block-copy kernel.
+* Freeing a sequence lowers the count of each of its blocks; blocks that
+  reach 0 go back to the free pool (studying-code.tistory.com/16, sections
+  "요청 완료 후 메모리 관리" and "물리적 블록 해제와 참조 카운트").  They are
+  returned last block first, as in the prefix-cache timeline of the itan.pw
+  page (time 4: a finished request's blocks enter the free queue in reverse
+  order), and appended at the tail of the FIFO free list (the front is where
+  ``pop(0)`` takes new blocks in tech.blogsailing.com/?p=100).
+* Running out of free blocks is reported and leaves the state unchanged.
+"""
+from __future__ import annotations
+
+from collections import deque
+
+
+class OutOfBlocks(Exception):
+    pass
+
+
+class PoolReplay:
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        if num_blocks < 0 or block_size <= 0:
+            raise ValueError("bad pool geometry")
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise ValueError("free_order must be a permutation of the block ids")
+        self.free = deque(order)
+        self.ref = [0] * num_blocks
+        self.tables: dict[int, list[int]] = {}
+        self.lens: dict[int, int] = {}
+        self.next_id = 0
+
+    # -- operations -------------------------------------------------------
+    def add_seq(self, num_tokens: int) -> int:
+        need = -(-num_tokens // self.block_size)
+        if need > len(self.free):
+            raise OutOfBlocks()
+        blocks = [self.free.popleft() for _ in range(need)]
+        for b in blocks:
+            self.ref[b] = 1
+        sid = self.next_id
+        self.next_id += 1
+        self.tables[sid] = blocks
+        self.lens[sid] = num_tokens
+        return sid
+
+    def fork(self, parent: int) -> int:
+        blocks = list(self.tables[parent])
+        for b in blocks:
+            self.ref[b] += 1
+        sid = self.next_id
+        self.next_id += 1
+        self.tables[sid] = blocks
+        self.lens[sid] = self.lens[parent]
+        return sid
+
+    def append_token(self, sid: int):
+        """Returns (slot, pair) where pair is (src, dst) of a copy-on-write or None."""
+        table = self.tables[sid]
+        pos = self.lens[sid]
+        logical, offset = divmod(pos, self.block_size)
+        pair = None
+        if logical == len(table):
+            if not self.free:
+                raise OutOfBlocks()
+            b = self.free.popleft()
+            self.ref[b] = 1
+            table.append(b)
+        else:
+            b = table[logical]
+            if self.ref[b] > 1:
+                if not self.free:
+                    raise OutOfBlocks()
+                nb = self.free.popleft()
+                self.ref[nb] = 1
+                self.ref[b] -= 1
+                table[logical] = nb
+                pair = (b, nb)
+                b = nb
+        self.lens[sid] = pos + 1
+        return b * self.block_size + offset, pair
+
+    def free_seq(self, sid: int) -> None:
+        for b in reversed(self.tables.pop(sid)):
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+        del self.lens[sid]
+
+    # -- views -------------------------------------------------------------
+    def table(self, sid: int):
+        return list(self.tables[sid]), self.lens[sid]
+
+    def filled(self, sid: int):
+        """#filled of every block-table entry (the pages' per-entry fill count)."""
+        n, bs = self.lens[sid], self.block_size
+        return [min(bs, n - i * bs) for i in range(len(self.tables[sid]))]
+
+    def slot(self, sid: int, pos: int) -> int:
+        return self.tables[sid][pos // self.block_size] * self.block_size + pos % self.block_size
+
+    def num_free(self) -> int:
+        return len(self.free)
+
+    def check_invariants(self) -> None:
+        used = [b for b in range(self.num_blocks) if self.ref[b] > 0]
+        assert set(used).isdisjoint(self.free), "block both used and free"
+        assert len(used) + len(self.free) == self.num_blocks, "block lost"
+        assert len(set(self.free)) == len(self.free), "block twice in the free list"
+        total_refs = sum(self.ref)
+        total_entries = sum(len(t) for t in self.tables.values())
+        assert total_refs == total_entries, "ref counts disagree with the tables"
