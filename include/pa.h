@@ -1,0 +1,245 @@
+/*
+ * pa.h -- C ABI of the GB300 paged KV-cache library (libpa.so).
+ *
+ * One layer's KV cache is a single device buffer laid out as
+ *
+ *     cache[2][num_blocks][block_size][num_kv_heads][head_size]
+ *
+ * with index 0 of the first axis holding keys and 1 values.  This is the
+ * per-layer tensor the itan.pw page ("vLLMにおけるKVCacheマネージャーの詳細解説",
+ * sections "ブロックアロケーションの基本概念" and "BlockPoolの生成過程")
+ * allocates for every attention layer: num_blocks physical blocks of
+ * block_size token slots each.  A sequence reaches its tokens through a block
+ * table that maps logical block i to a physical block (studying-code.tistory.com/16,
+ * section "vLLM 방식: 논리 ↔ 물리 메모리 분리").  Token j of a sequence lives
+ * in slot  table[j / block_size] * block_size + j % block_size.
+ *
+ * Conventions for every call below
+ *   - Device pointers are plain CUDA device addresses the caller allocated;
+ *     the library never allocates, frees or synchronises device memory except
+ *     where a call says so.  Host pointers are ordinary process memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Kernel calls are asynchronous on that stream.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns PA_ERR_INVALID_ARG (or PA_ERR_UNSUPPORTED for a valid shape this
+ *     build has no kernel for) and launches nothing.  A failed launch returns
+ *     PA_ERR_CUDA.
+ *   - Index errors that only the device can see (a slot, block id or
+ *     sequence length outside the pool or table) are recorded in a per-device
+ *     error word and the offending access is skipped; nothing traps.  Read
+ *     the word with pa_get_device_error().
+ *   - dtype (pa_cache_desc.dtype) is the element type of the cache and of
+ *     every key, value, query and output tensor of the call.  Arithmetic is
+ *     fp32 in both cases.
+ */
+#ifndef PAGED_KV_CACHE_PA_H_
+#define PAGED_KV_CACHE_PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,    /* null pointer, bad size or inconsistent shape */
+  PA_ERR_UNSUPPORTED = 2,    /* valid, but no kernel in this build (head size, group) */
+  PA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+  PA_ERR_OUT_OF_BLOCKS = 4,  /* block pool exhausted; pool state unchanged */
+  PA_ERR_BAD_STATE = 5,      /* unknown sequence id, or an operation the state forbids */
+  PA_ERR_DEVICE_CHECK = 6,   /* pa_get_device_error found a recorded device-side error */
+  PA_ERR_TIMEOUT = 7         /* a bounded device wait gave up (see pa_get_device_error) */
+} pa_status;
+
+typedef enum pa_dtype { PA_BF16 = 0, PA_FP32 = 1 } pa_dtype;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_SLOT 0x1u        /* reshape_and_cache: slot >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_ID 0x2u    /* decode / copy_blocks: block id outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 0x4u     /* decode: seq_len > max_seq_len or > table capacity */
+#define PA_DEVERR_TIMEOUT 0x8u     /* a pipeline wait exceeded its limit (about 1 s) */
+
+/* Geometry of one layer's cache. */
+typedef struct pa_cache_desc {
+  int32_t num_blocks;    /* physical blocks in the pool, >= 1 */
+  int32_t block_size;    /* token slots per block: a power of two in [1, 256] */
+  int32_t num_kv_heads;  /* KV heads, >= 1 */
+  int32_t head_size;     /* elements per head: 64, 128 or 256 */
+  int32_t dtype;         /* pa_dtype */
+} pa_cache_desc;
+
+/* ---------------------------------------------------------------------------
+ * Cache write.  Each new token's key and value go to the physical slot that
+ * slot_mapping names (itan.pw page, section "ブロックアロケーションの基本概念":
+ * slot_mapping records, for every new token, its slot in the physical KV cache;
+ * studying-code.tistory.com/16, section "디코딩 과정": new KV is stored into
+ * physical blocks during each iteration):
+ *     cache[0][slot / block_size][slot % block_size][h][:] = key[t][h][:]
+ *     cache[1][slot / block_size][slot % block_size][h][:] = value[t][h][:]
+ *   cache         device, in/out, the layer's pool.
+ *   key, value    device, [num_tokens][num_kv_heads][head_size], contiguous.
+ *   slot_mapping  device int64 [num_tokens]; slot < 0 marks a padding token
+ *                 that is skipped.  Slots must be distinct (two tokens writing
+ *                 one slot leave either value).  A slot past the pool is
+ *                 skipped and recorded as PA_DEVERR_SLOT.
+ * Result is bit-exact: a byte copy.  num_tokens == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache(void* cache, const pa_cache_desc* desc, const void* key,
+                               const void* value, const int64_t* slot_mapping,
+                               int32_t num_tokens, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Copy-on-write block copies.  For each pair i, physical block
+ * pairs[2i] (source) is copied to block pairs[2i+1] (destination), keys and
+ * values, bit-exactly (studying-code.tistory.com/16, section "생성 단계에서의
+ * Copy-on-Write": the writer of a shared block takes a new block and copies
+ * the old block's content into it; section "메모리 복사 오버헤드의 최적화":
+ * only that one block is copied).
+ *   pairs   device int64 [num_pairs][2].  Destinations must be distinct and
+ *           no destination may also be a source in the same call (the pool
+ *           only emits fresh destinations).  An id outside the pool skips the
+ *           pair and records PA_DEVERR_BLOCK_ID.
+ * num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* pairs,
+                         int32_t num_pairs, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention: one query token per sequence against the
+ * sequence's cached tokens, block by block through its block table
+ * (studying-code.tistory.com/16, section "PagedAttention: 운영체제의 페이징
+ * 개념에서 영감을 받은 새로운 어텐션 알고리즘": the query is multiplied with each
+ * block's keys and values and the per-block results are combined into o_i;
+ * garden.houmin.site/infra/paged-attention, section "KV Cache 管理器").  The
+ * pages print no softmax or scale; the operation is the standard one:
+ *
+ *   out[s][hq][:] = sum_j softmax_j(scale * q[s][hq] . k_j) v_j,  j < seq_lens[s],
+ *   k_j = cache[0][table[s][j / bs]][j % bs][hq / G][:],  v_j likewise at index 1,
+ *   G = num_heads / num_kv_heads (query heads hq = h*G .. h*G+G-1 share KV head h).
+ *
+ *   out          device [num_seqs][num_heads][head_size], dtype.
+ *   query        device [num_seqs][num_heads][head_size], dtype.
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                ceil(seq_lens[s] / block_size) entries of row s are read.
+ *   seq_lens     device int32 [num_seqs]; the count includes the token just
+ *                written.  0 gives a zero output row.
+ *   max_seq_len  host bound on every seq_lens[s] (sizes the split grid).
+ *   partition_size  0: one CTA per (sequence, KV head) walks the whole
+ *                sequence.  > 0: split-KV, tokens cut into partitions of this
+ *                many tokens (a multiple of block_size), each reduced to a
+ *                partial (max, sum, weighted values) in workspace, then
+ *                combined by a log-sum-exp reduce kernel.  -1: the library
+ *                picks (pa_decode_partition_size reports the choice).
+ *   workspace    device scratch of at least pa_decode_workspace_size() bytes,
+ *                256-byte aligned; may be NULL when that size is 0.  Its
+ *                contents need no initialisation and are clobbered.
+ * G must be in 1..8.  Grouped heads share each K/V block load.
+ * Arithmetic: fp32 dot products and an online fp32 softmax; bf16 output is
+ * rounded to nearest even.  A sequence longer than max_seq_len or than its
+ * table row is recorded as PA_DEVERR_SEQ_LEN and its row is left undefined.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
+                    int32_t max_seq_len, int32_t partition_size, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* The partition size pa_decode uses for these arguments (0 = no split). */
+pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
+                                   int32_t num_heads, int32_t max_seq_len,
+                                   int32_t partition_size, int32_t* resolved);
+
+/* Workspace bytes pa_decode needs for these arguments (0 when it does not split):
+ * num_seqs * num_heads * max_partitions * (head_size + 1) * 4, rounded up to 256. */
+pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
+                                   int32_t num_heads, int32_t max_seq_len,
+                                   int32_t partition_size, size_t* bytes);
+
+/* ---------------------------------------------------------------------------
+ * Slot mapping from block tables (host).  slots[i] is the physical slot of
+ * token positions[i] of sequence seq_idx[i]:
+ *   table[seq][pos / block_size] * block_size + pos % block_size
+ * (tech.blogsailing.com/?p=100, section 2: a token index splits into the
+ * logical block token_idx // BLOCK_SIZE and the offset token_idx % BLOCK_SIZE;
+ * the block table maps the logical block to a physical one).
+ * All arrays are host memory; block_tables is [num_seqs][max_blocks_per_seq].
+ * Returns PA_ERR_INVALID_ARG if a sequence index falls outside [0, num_seqs),
+ * a position outside its table row or a table entry outside [0, num_blocks).
+ * ------------------------------------------------------------------------- */
+pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
+                          int32_t max_blocks_per_seq, int32_t block_size, int32_t num_blocks,
+                          const int32_t* seq_idx, const int32_t* positions, int32_t n,
+                          int64_t* slots);
+
+/* ---------------------------------------------------------------------------
+ * Host block pool: the block bookkeeping that produces block tables, slot
+ * mappings and copy-on-write pairs.  Host memory only; not thread-safe (one
+ * pool per scheduler thread).  Rules (studying-code.tistory.com/16, sections
+ * "물리적 블록 할당", "요청 완료 후 메모리 관리", the two-sample example and
+ * "생성 단계에서의 Copy-on-Write"; tech.blogsailing.com/?p=100, section 3;
+ * itan.pw page, section "ブロック割当のロジック"):
+ *   - a prompt of n tokens takes ceil(n / block_size) blocks from the front of
+ *     a FIFO free list; later tokens fill the last block and a new block is
+ *     taken only when it is full;
+ *   - fork shares every block of the parent and raises its reference count;
+ *   - a token written into a block whose count is above 1 first moves the
+ *     sequence to a new block: the old block's count drops by one and a
+ *     (src, dst) pair is reported for pa_copy_blocks; a holder that finds the
+ *     count at 1 writes in place;
+ *   - freeing a sequence lowers the count of each block, last block first,
+ *     and blocks at 0 go to the tail of the free list;
+ *   - a call that runs out of free blocks returns PA_ERR_OUT_OF_BLOCKS and
+ *     leaves the pool exactly as it was.
+ * Sequence ids count up from 0 in creation order and are never reused.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_pool pa_pool;
+
+/* free_order: NULL for 0..num_blocks-1, else a permutation of the block ids
+ * giving the initial order of the free list (front first). */
+pa_status pa_pool_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                         pa_pool** out);
+void pa_pool_destroy(pa_pool* pool);
+/* New sequence holding num_tokens (>= 0) prompt tokens. */
+pa_status pa_pool_add_seq(pa_pool* pool, int64_t num_tokens, int64_t* seq_id);
+/* New sequence sharing all of parent's blocks and its length. */
+pa_status pa_pool_fork(pa_pool* pool, int64_t parent, int64_t* child);
+/* Reserve the slot of the sequence's next token.  cow_pair receives the
+ * (src, dst) copy to run before the write, or (-1, -1). */
+pa_status pa_pool_append_token(pa_pool* pool, int64_t seq, int64_t* slot, int64_t cow_pair[2]);
+/* append_token for n sequences in order, all or nothing.  slots: [n];
+ * cow_pairs: room for [n][2]; *num_pairs receives how many pairs were written. */
+pa_status pa_pool_append_tokens(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* slots,
+                                int64_t* cow_pairs, int32_t* num_pairs);
+pa_status pa_pool_free_seq(pa_pool* pool, int64_t seq);
+/* Block table of seq: up to cap entries into out; *num_table_blocks and
+ * *seq_len receive the table length and the token count. */
+pa_status pa_pool_block_table(const pa_pool* pool, int64_t seq, int32_t* out, int32_t cap,
+                              int32_t* num_table_blocks, int64_t* seq_len);
+/* Dense [n][max_blocks_per_seq] tables and lengths for n sequences (unused
+ * entries 0), ready to copy to the device for pa_decode. */
+pa_status pa_pool_fill_tables(const pa_pool* pool, const int64_t* seqs, int32_t n,
+                              int32_t* block_tables, int32_t max_blocks_per_seq,
+                              int32_t* seq_lens);
+/* Slot of token pos (< seq_len) of seq. */
+pa_status pa_pool_slot(const pa_pool* pool, int64_t seq, int64_t pos, int64_t* slot);
+pa_status pa_pool_ref_count(const pa_pool* pool, int32_t block, int32_t* ref);
+int32_t pa_pool_num_free(const pa_pool* pool);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics.
+ * pa_get_device_error synchronises `stream`, returns the current device's
+ * error word (PA_DEVERR_* bits) in *flags and clears it.  Returns
+ * PA_ERR_DEVICE_CHECK when a bit was set, PA_OK otherwise.
+ * ------------------------------------------------------------------------- */
+pa_status pa_get_device_error(uint32_t* flags, void* stream);
+const char* pa_status_string(pa_status status);
+/* Library version, e.g. "0.1.0". */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_CACHE_PA_H_ */

@@ -1,0 +1,353 @@
+// C ABI of the library: argument checks, TMA descriptor encoding, launch
+// geometry and kernel dispatch.  See include/pa.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "decode_kernel.cuh"
+#include "pa.h"
+#include "pa_launch.h"
+
+// Per-device error word written by the kernels (PA_DEVERR_* bits); static
+// storage, so it starts at zero on every device that loads the library.
+__device__ unsigned int g_pa_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kStageBudgetBytes = 96 * 1024;  // shared memory for the K/V stage ring
+constexpr int kMaxSmemPerCta = 227 * 1024;
+
+std::mutex g_mutex;
+unsigned int* g_error_word[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+int elem_bytes(int dtype) { return dtype == PA_BF16 ? 2 : 4; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Device-side state of the current device: the error word's address and the SM count.
+pa_status device_state(unsigned int** err, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_error_word[dev]) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_pa_error_word) != cudaSuccess) return PA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    g_num_sms[dev] = sms;
+    g_error_word[dev] = static_cast<unsigned int*>(addr);
+  }
+  if (err) *err = g_error_word[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
+  return PA_OK;
+}
+
+pa_status encode_fn(EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return PA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = g_encode;
+  return PA_OK;
+}
+
+pa_status check_desc(const pa_cache_desc* d) {
+  if (!d) return PA_ERR_INVALID_ARG;
+  if (d->num_blocks < 1 || d->num_kv_heads < 1 || d->head_size < 1) return PA_ERR_INVALID_ARG;
+  if (!is_pow2(d->block_size) || d->block_size > 256) return PA_ERR_INVALID_ARG;
+  if (d->dtype != PA_BF16 && d->dtype != PA_FP32) return PA_ERR_INVALID_ARG;
+  if ((d->head_size * elem_bytes(d->dtype)) % 16 != 0) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+bool head_size_supported(int d) { return d == 64 || d == 128 || d == 256; }
+
+// Partition policy.  An explicit size is checked; -1 picks the largest of
+// 512, 256, 128, 64 tokens (not below the block size) that still gives about
+// three CTAs per SM when sequences average half of max_seq_len.  A size that
+// covers max_seq_len means no split (0).
+pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int max_seq_len,
+                            int requested, int num_sms, int* out) {
+  int p = requested;
+  if (p == -1) {
+    p = 512;
+    const long long heads = (long long)num_seqs * d->num_kv_heads;
+    while (p > 64 && p > d->block_size &&
+           heads * ((max_seq_len + p - 1) / p) < 6LL * num_sms)
+      p >>= 1;
+    if (p < d->block_size) p = d->block_size;
+  } else if (p < -1) {
+    return PA_ERR_INVALID_ARG;
+  } else if (p > 0 && p % d->block_size != 0) {
+    return PA_ERR_INVALID_ARG;
+  }
+  if (p > 0 && max_seq_len <= p) p = 0;
+  *out = p;
+  return PA_OK;
+}
+
+size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_parts) {
+  const size_t rows = (size_t)num_seqs * num_heads * max_parts;
+  size_t o_bytes = rows * head_size * 4;
+  o_bytes = (o_bytes + 255) / 256 * 256;
+  size_t lse_bytes = (rows * 4 + 255) / 256 * 256;
+  return o_bytes + lse_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_version(void) { return "0.1.0"; }
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_OUT_OF_BLOCKS: return "out of blocks";
+    case PA_ERR_BAD_STATE: return "bad state";
+    case PA_ERR_DEVICE_CHECK: return "device-side check failed";
+    case PA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+pa_status pa_get_device_error(uint32_t* flags, void* stream) {
+  if (!flags) return PA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  pa_status st = device_state(&err, nullptr);
+  if (st != PA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned int zero = 0;
+  if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return PA_ERR_CUDA;
+  *flags = v;
+  if (v & PA_DEVERR_TIMEOUT) return PA_ERR_TIMEOUT;
+  return v ? PA_ERR_DEVICE_CHECK : PA_OK;
+}
+
+pa_status pa_reshape_and_cache(void* cache, const pa_cache_desc* desc, const void* key,
+                               const void* value, const int64_t* slot_mapping,
+                               int32_t num_tokens, void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!cache || !key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned(cache, 16) || !aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  if ((st = device_state(&err, nullptr)) != PA_OK) return st;
+  const int row_bytes = desc->num_kv_heads * desc->head_size * elem_bytes(desc->dtype);
+  const int64_t num_slots = (int64_t)desc->num_blocks * desc->block_size;
+  const int64_t plane_bytes = num_slots * row_bytes;
+  return cuda_status(pa::launch_reshape_and_cache(cache, key, value, slot_mapping, num_tokens,
+                                                  num_slots, row_bytes, plane_bytes, err,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* pairs,
+                         int32_t num_pairs, void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0 || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!cache || !pairs || !aligned(cache, 16) || !aligned(pairs, 8)) return PA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  if ((st = device_state(&err, nullptr)) != PA_OK) return st;
+  const int64_t block_bytes = (int64_t)desc->block_size * desc->num_kv_heads * desc->head_size *
+                              elem_bytes(desc->dtype);
+  const int64_t plane_bytes = block_bytes * desc->num_blocks;
+  return cuda_status(pa::launch_copy_blocks(cache, pairs, num_pairs, desc->num_blocks,
+                                            block_bytes, plane_bytes, err,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
+                                   int32_t num_heads, int32_t max_seq_len,
+                                   int32_t partition_size, int32_t* resolved) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (!resolved || num_seqs < 0 || max_seq_len < 0 || num_heads < 1) return PA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (partition_size == -1 && (st = device_state(nullptr, &sms)) != PA_OK) return st;
+  int p = 0;
+  if ((st = resolve_partition(desc, num_seqs, max_seq_len, partition_size, sms, &p)) != PA_OK)
+    return st;
+  *resolved = p;
+  return PA_OK;
+}
+
+pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
+                                   int32_t num_heads, int32_t max_seq_len,
+                                   int32_t partition_size, size_t* bytes) {
+  if (!bytes) return PA_ERR_INVALID_ARG;
+  int32_t p = 0;
+  pa_status st = pa_decode_partition_size(desc, num_seqs, num_heads, max_seq_len,
+                                          partition_size, &p);
+  if (st != PA_OK) return st;
+  *bytes = p == 0 ? 0
+                  : workspace_bytes_for(num_seqs, num_heads, desc->head_size,
+                                        (max_seq_len + p - 1) / p);
+  return PA_OK;
+}
+
+pa_status pa_decode(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
+                    int32_t max_seq_len, int32_t partition_size, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || num_heads < 1 || max_seq_len < 0 ||
+      max_blocks_per_seq < 1 || !std::isfinite(scale))
+    return PA_ERR_INVALID_ARG;
+  if (num_heads % desc->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !query || !cache || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
+  const int es = elem_bytes(desc->dtype);
+  if (!aligned(cache, 16) || !aligned(query, es) || !aligned(out, es) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PA_ERR_INVALID_ARG;
+  const int group = num_heads / desc->num_kv_heads;
+  if (!head_size_supported(desc->head_size) || group > 8) return PA_ERR_UNSUPPORTED;
+  if (desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+
+  unsigned int* err = nullptr;
+  int sms = 0;
+  if ((st = device_state(&err, &sms)) != PA_OK) return st;
+  int part = 0;
+  if ((st = resolve_partition(desc, num_seqs, max_seq_len, partition_size, sms, &part)) != PA_OK)
+    return st;
+  const int max_parts = part > 0 ? (max_seq_len + part - 1) / part : 1;
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (part > 0) {
+    const size_t need = workspace_bytes_for(num_seqs, num_heads, desc->head_size, max_parts);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+      return PA_ERR_INVALID_ARG;
+    part_o = static_cast<float*>(workspace);
+    size_t o_bytes = (size_t)num_seqs * num_heads * max_parts * desc->head_size * 4;
+    o_bytes = (o_bytes + 255) / 256 * 256;
+    part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
+  }
+
+  // Stage geometry: 32 tokens per stage, TMA boxes of min(block_size, 32)
+  // rows, one box per 128-byte column group, each box at a 1024-byte
+  // aligned slot so the 128-byte swizzle pattern starts on an atom.
+  const int D = desc->head_size;
+  const int BS = desc->block_size;
+  const int R = BS < pa::kStageTokens ? BS : pa::kStageTokens;
+  const int groups = D * es / 128;
+  const int gslot = R * 128 > 1024 ? R * 128 : 1024;
+  const int region = (pa::kStageTokens / R) * groups * gslot;
+  const int stage_bytes = 2 * region;
+  // As many stages as the budget holds (at most 64); at least two when two
+  // fit in a CTA's shared memory, else one (tiny blocks of long fp32 rows).
+  const int merge = pa::decode_merge_bytes(group, D);
+  auto area_for = [&](int n) {
+    const int a = n * stage_bytes;
+    return a < merge ? (merge + 15) / 16 * 16 : a;
+  };
+  int ns = kStageBudgetBytes / stage_bytes;
+  if (ns > 64) ns = 64;
+  if (ns < 2) ns = pa::decode_smem_bytes(area_for(2), group, D) <= kMaxSmemPerCta ? 2 : 1;
+  const int stage_area = area_for(ns);
+  const int smem = pa::decode_smem_bytes(stage_area, group, D);
+  if (smem > kMaxSmemPerCta) return PA_ERR_UNSUPPORTED;
+
+  EncodeTiledFn encode = nullptr;
+  if ((st = encode_fn(&encode)) != PA_OK) return st;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  const int inner = 128 / es;
+  const cuuint64_t gdim[5] = {(cuuint64_t)inner, (cuuint64_t)groups,
+                              (cuuint64_t)desc->num_kv_heads, (cuuint64_t)BS,
+                              2ull * (cuuint64_t)desc->num_blocks};
+  const cuuint64_t gstride[4] = {128ull, (cuuint64_t)D * es,
+                                 (cuuint64_t)desc->num_kv_heads * D * es,
+                                 (cuuint64_t)BS * desc->num_kv_heads * D * es};
+  const cuuint32_t box[5] = {(cuuint32_t)inner, 1u, 1u, (cuuint32_t)R, 1u};
+  const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult cr = encode(&map,
+                       desc->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       5, const_cast<void*>(cache), gdim, gstride, box, estride,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return PA_ERR_CUDA;
+
+  pa::DecodeParams prm;
+  prm.out = out;
+  prm.query = query;
+  prm.block_tables = block_tables;
+  prm.seq_lens = seq_lens;
+  prm.part_o = part_o;
+  prm.part_lse = part_lse;
+  prm.err = err;
+  prm.num_blocks = desc->num_blocks;
+  prm.block_size = BS;
+  prm.log2_block_size = ilog2(BS);
+  prm.num_kv_heads = desc->num_kv_heads;
+  prm.num_heads = num_heads;
+  prm.max_blocks_per_seq = max_blocks_per_seq;
+  prm.partition_tokens = part;
+  prm.max_parts = max_parts;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  prm.box_rows = R;
+  prm.log2_box_rows = ilog2(R);
+  prm.group_slot = gslot;
+  prm.region_bytes = region;
+  prm.num_stages = ns;
+  prm.stage_area = stage_area;
+
+  const dim3 grid((unsigned)max_parts, (unsigned)desc->num_kv_heads, (unsigned)num_seqs);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool supported = true;
+  cudaError_t e = desc->dtype == PA_BF16
+                      ? pa::launch_decode_bf16(D, group, grid, smem, s, map, prm, &supported)
+                      : pa::launch_decode_f32(D, group, grid, smem, s, map, prm, &supported);
+  if (!supported) return PA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (part > 0) {
+    e = pa::launch_lse_reduce(desc->dtype, D, out, part_o, part_lse, seq_lens, num_seqs,
+                              num_heads, part, max_parts, s, &supported);
+    if (!supported) return PA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

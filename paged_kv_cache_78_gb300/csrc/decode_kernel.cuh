@@ -1,0 +1,458 @@
+// Paged decode attention for sm_103a: TMA-staged K/V blocks, warp-level
+// online softmax, fp32 accumulation; split-KV partials and their
+// log-sum-exp reduce.
+//
+// The operation (studying-code.tistory.com/16, section "PagedAttention:
+// 운영체제의 페이징 개념에서 영감을 받은 새로운 어텐션 알고리즘"; garden.houmin.site/
+// infra/paged-attention, section "KV Cache 管理器"): the query of each sequence
+// meets the key block K_j and value block V_j of every logical block j, found
+// through the block table, and the per-block results are combined into o_i.
+// Scores are scale * q.k with a softmax over the sequence's tokens.
+//
+// Work decomposition (one CTA = one (partition, KV head, sequence)):
+//   warp 0      producer: walks the partition's block table (32 entries per
+//               lane-parallel load) and issues one TMA box per (block, 128-byte
+//               column group, K or V) into a ring of shared-memory stages of
+//               32 tokens, completing on the stage's "full" mbarrier;
+//   warps 1..4  consumers: warp w takes stages w, w+4, ...; per stage
+//               QK      lane j owns token j and computes all G = Hq/Hkv query
+//                       heads' scores (query heads of a GQA group share the K
+//                       load), reading the row through the 128-byte swizzle;
+//               softmax warp max per head, rescale factor 2^(m_old - m_new),
+//                       p_j = 2^(s_j - m_new) written to a per-warp buffer;
+//               PV      lane (chunk c, token group r) accumulates
+//                       p_j[g] * v_j[c*8 .. c*8+7] for tokens j = r mod R;
+//               then releases the stage ("empty" mbarrier) to the producer.
+//   end         per-warp (m, l, o) merged across warps by log-sum-exp and
+//               written as the final output or as a split-KV partial.
+// Scores live in the log2 domain: q is pre-multiplied by scale * log2(e) so
+// that exp(x - m) becomes 2^(x' - m').
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
+constexpr int kStageTokens = 32;
+constexpr int kPStride = 8;  // floats per token in the per-warp softmax-weight buffer
+
+struct DecodeParams {
+  void* out;                    // [S][Hq][D] of T (final rows)
+  const void* query;            // [S][Hq][D] of T
+  const int32_t* block_tables;  // [S][max_blocks_per_seq]
+  const int32_t* seq_lens;      // [S]
+  float* part_o;                // [S][Hq][max_parts][D]: normalised partial outputs
+  float* part_lse;              // [S][Hq][max_parts]: log2-domain log-sum-exp of each partial
+  unsigned int* err;            // device error word
+  int num_blocks;
+  int block_size;
+  int log2_block_size;
+  int num_kv_heads;
+  int num_heads;
+  int max_blocks_per_seq;
+  int partition_tokens;  // 0 = the whole sequence in one CTA
+  int max_parts;         // grid.x in split mode
+  float scale_log2;      // scale * log2(e)
+  // shared-memory geometry, bytes
+  int box_rows;          // tokens per TMA box: min(block_size, 32)
+  int log2_box_rows;
+  int group_slot;        // bytes per (box, 128-byte column group): max(box_rows*128, 1024)
+  int region_bytes;      // K (or V) part of one stage
+  int num_stages;
+  int stage_area;        // bytes before the query buffer (stages, or the merge overlay)
+};
+
+// Dynamic shared memory a decode launch needs (the kernel aligns its base to 1024).
+inline int decode_smem_bytes(int stage_area, int group, int head_size) {
+  int bytes = 1024 + stage_area;
+  bytes += group * head_size * 4;                      // pre-scaled fp32 query
+  bytes += kConsumerWarps * kStageTokens * kPStride * 4;  // softmax weights
+  bytes += 2 * 64 * 8;                                 // up to 64 stages x (full, empty)
+  bytes += 16;                                         // flags
+  return bytes;
+}
+
+// Bytes of the cross-warp merge overlay: m, l and o of every consumer warp.
+inline int decode_merge_bytes(int group, int head_size) {
+  return kConsumerWarps * group * (head_size + 2) * 4;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+  using E = ElemTraits<T>;
+  constexpr int kRowBytes = D * E::kBytes;
+  constexpr int kChunks = kRowBytes / 16;             // 16-byte chunks per token row
+  constexpr int kGroups = kRowBytes / 128;            // 128-byte column groups per row
+  constexpr int kEPC = E::kPerChunk;                  // elements per chunk
+  constexpr int kCPL = kChunks > 32 ? kChunks / 32 : 1;  // PV chunks per lane
+  constexpr int kRpv = kChunks >= 32 ? 1 : 32 / kChunks;  // PV token groups per warp
+  static_assert(kRowBytes % 128 == 0, "head rows must be whole 128-byte groups");
+  static_assert(G >= 1 && G <= kPStride, "group size");
+
+  const int part = blockIdx.x;
+  const int h = blockIdx.y;
+  const int s = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int L = p.seq_lens[s];
+  const int P = p.partition_tokens;
+  const bool split = P > 0;
+  const int nparts = L <= 0 ? 0 : (split ? (L + P - 1) / P : 1);
+  const size_t row0 = (size_t)s * p.num_heads + (size_t)h * G;  // first query row
+
+  if (L <= 0) {
+    if (part == 0) {
+      T* out = reinterpret_cast<T*>(p.out) + row0 * D;
+      for (int i = tid; i < G * D; i += blockDim.x) out[i] = E::from_float(0.f);
+    }
+    return;
+  }
+  if ((split && nparts > p.max_parts) ||
+      ((L + p.block_size - 1) >> p.log2_block_size) > p.max_blocks_per_seq) {
+    if (part == 0 && tid == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
+    return;
+  }
+  if (part >= nparts) return;
+
+  const int tok0 = split ? part * P : 0;
+  const int tok1 = split ? min(L, tok0 + P) : L;
+  const int n_stages = (tok1 - tok0 + kStageTokens - 1) / kStageTokens;
+  const int NS = p.num_stages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(base);
+  float* q_s = reinterpret_cast<float*>(base + p.stage_area);
+  float* p_all = q_s + G * D;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_all + kConsumerWarps * kStageTokens * kPStride);
+  volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * 64);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * NS;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8u * i, 1);
+      mbar_init(empty0 + 8u * i, 1);
+    }
+    flags[0] = 0;  // abort
+    flags[1] = 0;  // stages issued
+    fence_mbar_init();
+  }
+  if (tid == 32) tma_prefetch_desc(&kv_map);
+  {
+    const T* qg = reinterpret_cast<const T*>(p.query) + row0 * D;
+    for (int i = tid; i < G * D; i += blockDim.x) q_s[i] = E::to_float(qg[i]) * p.scale_log2;
+  }
+  __syncthreads();
+
+  const int R = p.box_rows;
+  const int log2R = p.log2_box_rows;
+  const int gslot = p.group_slot;
+  const int region = p.region_bytes;
+
+  // Consumer state (the producer warp leaves it unused).
+  float m_run[G], l_run[G];
+  float o[G][kCPL * kEPC];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = -INFINITY;
+    l_run[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kCPL * kEPC; ++e) o[g][e] = 0.f;
+  }
+  // PV lane roles: chunk index (first of kCPL) and token group.
+  const int pv_c = kChunks >= 32 ? lane : lane % kChunks;
+  const int pv_r = kChunks >= 32 ? 0 : lane / kChunks;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    const int BS = p.block_size;
+    const int l2bs = p.log2_block_size;
+    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+    const int lb_end = (tok1 + BS - 1) >> l2bs;  // one past the last logical block
+    int win = tok0 >> l2bs;                      // logical block held by lane 0 of `cur`
+    int cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
+    int nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+    const uint32_t box_bytes = (uint32_t)R * 128u;
+    int issued = 0;
+    for (int k = 0; k < n_stages; ++k) {
+      const int slot = k % NS;
+      if (k >= NS) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(empty0 + 8u * slot, ((k / NS) - 1) & 1, p.err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok || flags[0]) {
+          flags[0] = 1;
+          break;
+        }
+      }
+      const int st_tok = tok0 + k * kStageTokens;
+      const int st_n = min(kStageTokens, tok1 - st_tok);
+      const int nbox = (st_n + R - 1) >> log2R;
+      if (lane == 0)
+        mbar_arrive_expect_tx(full0 + 8u * slot, (uint32_t)(nbox * kGroups * 2) * box_bytes);
+      const uint32_t kdst = sbase + (uint32_t)slot * 2u * region;
+      for (int i = 0; i < nbox; ++i) {
+        const int tk = st_tok + (i << log2R);
+        const int lb = tk >> l2bs;
+        const int t0 = tk & (BS - 1);
+        while (lb >= win + 32) {
+          cur = nxt;
+          win += 32;
+          nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+        }
+        const int id = __shfl_sync(0xffffffffu, cur, lb - win);
+        if (lane == 0) {
+          int ck = id, cv = p.num_blocks + id;
+          if (id < 0 || id >= p.num_blocks) {
+            // Outside the tensor: the box reads the zero fill instead of another block.
+            record_error(p.err, PA_DEVERR_BLOCK_ID);
+            ck = cv = 2 * p.num_blocks;
+          }
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+            const uint32_t dst = kdst + (uint32_t)(i * kGroups + g) * gslot;
+            tma_load_5d(dst, &kv_map, full0 + 8u * slot, 0, g, h, t0, ck);
+            tma_load_5d(dst + region, &kv_map, full0 + 8u * slot, 0, g, h, t0, cv);
+          }
+        }
+      }
+      issued = k + 1;
+    }
+    if (lane == 0) flags[1] = issued;
+  } else {
+    // ---------------- consumers ----------------
+    const int w = warp - 1;
+    float* p_w = p_all + w * kStageTokens * kPStride;
+    const uint32_t p_w_s = smem_u32(p_w);
+    const uint32_t q_s_s = smem_u32(q_s);
+
+
+    // This lane's token in the QK phase and its row position inside a stage.
+    const int qk_box = lane >> log2R;
+    const int qk_t = lane & (R - 1);
+    const uint32_t qk_off = (uint32_t)(qk_box * kGroups) * gslot + (uint32_t)qk_t * 128u;
+    const uint32_t qk_swz = (uint32_t)(qk_t & 7);
+
+    for (int k = w; k < n_stages; k += kConsumerWarps) {
+      if (flags[0]) break;
+      const int slot = k % NS;
+      bool ok = mbar_wait_bounded(full0 + 8u * slot, (k / NS) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        flags[0] = 1;
+        break;
+      }
+      const int st_tok = tok0 + k * kStageTokens;
+      const int nvalid = min(kStageTokens, tok1 - st_tok);
+      const uint32_t kreg = sbase + (uint32_t)slot * 2u * region;
+      const uint32_t vreg = kreg + region;
+
+      // ---- scores: lane = token ----
+      float acc[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) acc[g] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t addr = kreg + qk_off + (uint32_t)(c >> 3) * gslot +
+                              ((((uint32_t)c & 7u) ^ qk_swz) << 4);
+        float kf[kEPC];
+        E::unpack(lds128(addr), kf);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int e4 = 0; e4 < kEPC; e4 += 4) {
+            const float4 qv = lds128f(q_s_s + (uint32_t)((g * D + c * kEPC + e4) * 4));
+            acc[g] = fmaf(qv.x, kf[e4 + 0], acc[g]);
+            acc[g] = fmaf(qv.y, kf[e4 + 1], acc[g]);
+            acc[g] = fmaf(qv.z, kf[e4 + 2], acc[g]);
+            acc[g] = fmaf(qv.w, kf[e4 + 3], acc[g]);
+          }
+        }
+      }
+      const bool valid = lane < nvalid;
+
+      // ---- online softmax over this stage (log2 domain) ----
+      float alpha[G];
+      float pj[kPStride];
+#pragma unroll
+      for (int g = 0; g < kPStride; ++g) pj[g] = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float sc = valid ? acc[g] : -INFINITY;
+        const float m_new = fmaxf(m_run[g], warp_max(sc));
+        alpha[g] = fast_exp2(m_run[g] - m_new);
+        m_run[g] = m_new;
+        pj[g] = fast_exp2(sc - m_new);
+        l_run[g] = fmaf(l_run[g], alpha[g], pj[g]);
+      }
+      {
+        float4* dst = reinterpret_cast<float4*>(p_w + lane * kPStride);
+        dst[0] = make_float4(pj[0], pj[1], pj[2], pj[3]);
+        if (G > 4) dst[1] = make_float4(pj[4], pj[5], pj[6], pj[7]);
+      }
+      __syncwarp();
+
+      // ---- values: lane = (chunk, token group) ----
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < kCPL * kEPC; ++e) o[g][e] *= alpha[g];
+      for (int j = pv_r; j < nvalid; j += kRpv) {
+        const int box = j >> log2R;
+        const int t = j & (R - 1);
+        const uint32_t rowbase = vreg + (uint32_t)(box * kGroups) * gslot + (uint32_t)t * 128u;
+        float pw[kPStride];
+        {
+          const float4 a = lds128f(p_w_s + (uint32_t)(j * kPStride * 4));
+          pw[0] = a.x; pw[1] = a.y; pw[2] = a.z; pw[3] = a.w;
+          if (G > 4) {
+            const float4 b = lds128f(p_w_s + (uint32_t)(j * kPStride * 4 + 16));
+            pw[4] = b.x; pw[5] = b.y; pw[6] = b.z; pw[7] = b.w;
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < kCPL; ++cc) {
+          const int c = pv_c + cc * 32;
+          const uint32_t addr = rowbase + (uint32_t)(c >> 3) * gslot +
+                                ((((uint32_t)c & 7u) ^ ((uint32_t)t & 7u)) << 4);
+          float vf[kEPC];
+          E::unpack(lds128(addr), vf);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < kEPC; ++e) o[g][cc * kEPC + e] = fmaf(pw[g], vf[e], o[g][cc * kEPC + e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+    }
+
+    // Per-warp totals: l over lanes, o over token groups.
+#pragma unroll
+    for (int g = 0; g < G; ++g) l_run[g] = warp_sum(l_run[g]);
+    if (kRpv > 1) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < kCPL * kEPC; ++e)
+#pragma unroll
+          for (int off = kChunks; off < 32; off <<= 1)
+            o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], off);
+    }
+  }
+  __syncthreads();  // (A) every stage consumed: the stage area is free for the merge
+  if (warp > 0 && !flags[0]) {
+    const int w = warp - 1;
+    float* Mw = reinterpret_cast<float*>(base);
+    float* Lw = Mw + kConsumerWarps * G;
+    float* Ow = Lw + kConsumerWarps * G;
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        Mw[w * G + g] = m_run[g];
+        Lw[w * G + g] = l_run[g];
+      }
+    }
+    if (pv_r == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int cc = 0; cc < kCPL; ++cc)
+#pragma unroll
+          for (int e = 0; e < kEPC; ++e)
+            Ow[(w * G + g) * D + (pv_c + cc * 32) * kEPC + e] = o[g][cc * kEPC + e];
+    }
+  }
+
+  if (flags[0]) {
+    // A wait gave up.  Before leaving, wait (bounded) for every TMA load this
+    // CTA issued, so that no copy into its shared memory is still in flight.
+    if (tid == 0) {
+      const int issued = flags[1];
+      for (int sl = 0; sl < NS && sl < issued; ++sl) {
+        const int last_use = (issued - 1 - sl) / NS;
+        mbar_wait_bounded(full0 + 8u * sl, last_use & 1, p.err);
+      }
+    }
+    return;
+  }
+  __syncthreads();  // (B) merge data written
+
+  {
+    const float* Mw = reinterpret_cast<const float*>(base);
+    const float* Lw = Mw + kConsumerWarps * G;
+    const float* Ow = Lw + kConsumerWarps * G;
+    for (int i = tid; i < G * D; i += blockDim.x) {
+      const int g = i / D;
+      const int d = i - g * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, Mw[w * G + g]);
+      float lsum = 0.f, osum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float sc = fast_exp2(Mw[w * G + g] - M);
+        lsum = fmaf(Lw[w * G + g], sc, lsum);
+        osum = fmaf(Ow[(w * G + g) * D + d], sc, osum);
+      }
+      const float val = osum / lsum;
+      if (nparts == 1) {
+        reinterpret_cast<T*>(p.out)[(row0 + g) * D + d] = E::from_float(val);
+      } else {
+        const size_t prow = (row0 + g) * (size_t)p.max_parts + part;
+        p.part_o[prow * D + d] = val;
+        if (d == 0) p.part_lse[prow] = M + log2f(lsum);
+      }
+    }
+  }
+}
+
+// Log-sum-exp combination of split-KV partials:
+//   M = max_p lse_p,  w_p = 2^(lse_p - M),  out = sum_p w_p o_p / sum_p w_p.
+// One CTA per (query head, sequence); one thread per output element.
+template <typename T, int D>
+__global__ void __launch_bounds__(D)
+    lse_reduce_kernel(void* out_, const float* __restrict__ part_o,
+                      const float* __restrict__ part_lse, const int32_t* __restrict__ seq_lens,
+                      int num_heads, int partition_tokens, int max_parts) {
+  using E = ElemTraits<T>;
+  const int hq = blockIdx.x;
+  const int s = blockIdx.y;
+  const int d = threadIdx.x;
+  const int L = seq_lens[s];
+  const int nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
+  if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
+  const size_t row = (size_t)s * num_heads + hq;
+  const float* lse = part_lse + row * max_parts;
+  const float* po = part_o + row * max_parts * D;
+  float M = -INFINITY;
+  for (int q = 0; q < nparts; ++q) M = fmaxf(M, lse[q]);
+  float wsum = 0.f, acc = 0.f;
+  for (int q = 0; q < nparts; ++q) {
+    const float w = fast_exp2(lse[q] - M);
+    wsum += w;
+    acc = fmaf(w, po[(size_t)q * D + d], acc);
+  }
+  reinterpret_cast<T*>(out_)[row * D + d] = E::from_float(acc / wsum);
+}
+
+}  // namespace pa

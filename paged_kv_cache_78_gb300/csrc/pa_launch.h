@@ -1,0 +1,36 @@
+// Host-side launchers shared by the C-ABI translation unit and the kernel
+// translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct DecodeParams;
+
+cudaError_t launch_reshape_and_cache(void* cache, const void* key, const void* value,
+                                     const int64_t* slot_mapping, int64_t num_tokens,
+                                     int64_t num_slots, int row_bytes, int64_t plane_bytes,
+                                     unsigned int* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* cache, const int64_t* pairs, int num_pairs,
+                               int64_t num_blocks, int64_t block_bytes, int64_t plane_bytes,
+                               unsigned int* err, cudaStream_t stream);
+
+// Decode launchers, one per element type.  `supported` is set to false (and
+// nothing launched) when no kernel exists for (head_size, group).
+cudaError_t launch_decode_bf16(int head_size, int group, dim3 grid, int smem_bytes,
+                               cudaStream_t stream, const CUtensorMap& map,
+                               const DecodeParams& params, bool* supported);
+cudaError_t launch_decode_f32(int head_size, int group, dim3 grid, int smem_bytes,
+                              cudaStream_t stream, const CUtensorMap& map,
+                              const DecodeParams& params, bool* supported);
+
+cudaError_t launch_lse_reduce(int dtype, int head_size, void* out, const float* part_o,
+                              const float* part_lse, const int32_t* seq_lens, int num_seqs,
+                              int num_heads, int partition_tokens, int max_parts,
+                              cudaStream_t stream, bool* supported);
+
+}  // namespace pa

@@ -1,0 +1,126 @@
+"""GPU parity of paged decode attention against the oracle: every head size,
+query-group size and block size the library supports, ragged tails, zero and
+one-token sequences, split-KV with many partitions, garbage in stale slots,
+block relabelling, and device-side error recording."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_78_gb300 as pa
+import workloads
+from gpu_util import DeviceCase, assert_close, oracle_reference, to_device, to_f64, to_host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(a):
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+@pytest.fixture(autouse=True)
+def clean_error_word():
+    pa.pa_get_device_error()
+    yield
+
+
+def check(case, partitions=(0, -1)):
+    ref, cache_ref = oracle_reference(case)
+    for p in partitions:
+        dc = DeviceCase(case)
+        out = dc.step(p)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
+        assert_close(to_f64(out), ref, case.dtype, "%s partition=%s" % (case.name, p))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_tiny_config(dtype):
+    check(workloads.tiny(dtype), partitions=(0, 16, 32, -1))
+
+
+# (Hq, Hkv, head_size, block_size, lengths, dtype, partitions)
+SHAPES = [
+    (14, 2, 64, 16, [1, 15, 16, 17, 33, 255, 700], "bf16", (0, 64)),
+    (4, 4, 128, 8, [0, 1, 31, 32, 33, 129], "bf16", (0, 32)),
+    (32, 8, 128, 16, [5, 100, 511, 512, 513, 1500], "bf16", (0, 512, 128)),
+    (32, 8, 128, 16, [7, 300, 1029], "fp32", (0, 256)),
+    (8, 1, 256, 32, [3, 64, 200], "bf16", (0, 64)),
+    (8, 1, 256, 32, [3, 64, 200], "fp32", (0, 96)),
+    (6, 2, 64, 1, [1, 2, 45, 90], "bf16", (0, 8)),
+    (4, 2, 128, 2, [3, 40], "fp32", (0, 16)),
+    (10, 2, 64, 64, [63, 64, 65, 300], "bf16", (0, 128)),
+    (3, 1, 128, 128, [1, 127, 128, 260], "bf16", (0, 256)),
+    (2, 1, 64, 256, [255, 256, 257, 600], "fp32", (0, 256)),
+    (9, 3, 64, 4, [17, 41], "bf16", (0, 8)),
+    (5, 1, 128, 16, [77], "bf16", (0, 16)),
+    (12, 2, 256, 16, [150, 33], "bf16", (0, 32)),
+    (40, 40, 128, 16, [1, 2048], "bf16", (0, 512)),
+    (16, 2, 64, 16, [5000], "bf16", (32, 256)),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lens,dtype,parts", SHAPES,
+                         ids=["hq%d_hkv%d_d%d_bs%d_%s" % (s[0], s[1], s[2], s[3], s[5])
+                              for s in SHAPES])
+def test_decode_shapes(hq, hkv, d, bs, lens, dtype, parts):
+    case = workloads.custom(len(lens), hq, hkv, d, bs, lens, dtype,
+                            seed=hq * 1000 + d + bs, cache_fill="garbage")
+    check(case, partitions=parts)
+
+
+def test_block_relabelling_gives_identical_output():
+    case = workloads.custom(3, 8, 2, 128, 16, [70, 300, 33], "bf16", seed=3)
+    a = DeviceCase(case).step(0).clone()
+    perm = np.random.default_rng(2).permutation(case.num_blocks)
+    case2 = workloads.custom(3, 8, 2, 128, 16, [70, 300, 33], "bf16", seed=3)
+    case2.block_tables = perm[case.block_tables].astype(np.int32)
+    b = DeviceCase(case2).step(0)
+    assert torch.equal(a, b)
+
+
+def test_repeated_calls_are_deterministic():
+    case = workloads.custom(4, 14, 2, 64, 16, [100, 900, 2000, 1], "bf16", seed=8)
+    dc = DeviceCase(case)
+    a = dc.step(128).clone()
+    b = dc.step(128).clone()
+    assert torch.equal(a, b)
+
+
+def test_bad_block_id_is_recorded_and_reads_zeros():
+    case = workloads.custom(2, 4, 4, 64, 16, [40, 20], "bf16", seed=4, cache_fill="zeros")
+    case.block_tables[0, 1] = case.num_blocks + 3
+    dc = DeviceCase.__new__(DeviceCase)
+    dc.case, dc.device = case, "cuda"
+    cache = oracle.fill_cache(workloads.custom(2, 4, 4, 64, 16, [40, 20], "bf16", seed=4,
+                                               cache_fill="zeros"))
+    dc.cache = to_device(cache)
+    bt = to_device(case.block_tables)
+    out = torch.empty_like(to_device(case.query))
+    pa.pa_decode(out, to_device(case.query), dc.cache, bt, to_device(case.seq_lens),
+                 case.scale, case.max_seq_len, 0, None)
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_BLOCK_ID
+    assert torch.isfinite(out).all()
+    # sequence 1 is untouched by the bad entry
+    ref = oracle.decode(case.query[1:], cache, case.block_tables[1:], case.seq_lens[1:], case.scale)
+    assert_close(to_f64(out[1:]), ref, "bf16")
+
+
+def test_seq_len_beyond_table_is_recorded():
+    case = workloads.custom(2, 4, 4, 64, 16, [40, 20], "bf16", seed=6, max_blocks=3)
+    dc = DeviceCase(case)
+    sl = torch.tensor([40, 49], dtype=torch.int32, device="cuda")   # 49 > 3 * 16
+    pa.pa_decode(dc.out, dc.query, dc.cache, dc.block_tables, sl, case.scale, 49, 0, None)
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_SEQ_LEN
+
+
+def test_decode_on_side_stream():
+    case = workloads.custom(3, 8, 2, 64, 16, [10, 400, 77], "bf16", seed=12)
+    ref, _ = oracle_reference(case)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dc = DeviceCase(case)
+        out = dc.step(64)
+    s.synchronize()
+    assert_close(to_f64(out), ref, "bf16")
