@@ -63,7 +63,7 @@ class CacheDesc(ctypes.Structure):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libpa.so is not built (%s); run paged_kv_cache_78_gb300._build.build()"
+        raise ImportError("libpa.so is not built (%s); run python paged_kv_cache_78_gb300/_build.py"
                           % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float

@@ -281,9 +281,14 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
     const int a = n * stage_bytes;
     return a < merge ? (merge + 15) / 16 * 16 : a;
   };
+  // Every ring slot belongs to one consumer warp, so the stage count is a
+  // multiple of the consumer count: 4 consumers with 4, 8, ... stages, or
+  // 1-3 consumers with as many stages when fewer fit.
   int ns = kStageBudgetBytes / stage_bytes;
   if (ns > 64) ns = 64;
   if (ns < 2) ns = pa::decode_smem_bytes(area_for(2), group, D) <= kMaxSmemPerCta ? 2 : 1;
+  if (ns >= pa::kConsumerWarps) ns -= ns % pa::kConsumerWarps;
+  const int consumers = ns < pa::kConsumerWarps ? ns : pa::kConsumerWarps;
   const int stage_area = area_for(ns);
   const int smem = pa::decode_smem_bytes(stage_area, group, D);
   if (smem > kMaxSmemPerCta) return PA_ERR_UNSUPPORTED;
@@ -331,6 +336,7 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
   prm.group_slot = gslot;
   prm.region_bytes = region;
   prm.num_stages = ns;
+  prm.num_consumers = consumers;
   prm.stage_area = stage_area;
 
   const dim3 grid((unsigned)max_parts, (unsigned)desc->num_kv_heads, (unsigned)num_seqs);

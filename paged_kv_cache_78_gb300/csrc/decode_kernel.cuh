@@ -14,7 +14,10 @@
 //               lane-parallel load) and issues one TMA box per (block, 128-byte
 //               column group, K or V) into a ring of shared-memory stages of
 //               32 tokens, completing on the stage's "full" mbarrier;
-//   warps 1..4  consumers: warp w takes stages w, w+4, ...; per stage
+//   warps 1..4  consumers: warp w takes stages w, w+C, ... (C consumer warps,
+//               C dividing the number of stages, so that every ring slot has
+//               a single owner and each slot's barrier phases are waited on in
+//               order; a parity wait can only tell apart adjacent phases); per stage
 //               QK      lane j owns token j and computes all G = Hq/Hkv query
 //                       heads' scores (query heads of a GQA group share the K
 //                       load), reading the row through the 128-byte swizzle;
@@ -60,7 +63,8 @@ struct DecodeParams {
   int log2_box_rows;
   int group_slot;        // bytes per (box, 128-byte column group): max(box_rows*128, 1024)
   int region_bytes;      // K (or V) part of one stage
-  int num_stages;
+  int num_stages;        // a multiple of num_consumers
+  int num_consumers;     // consumer warps that take stages (1..kConsumerWarps)
   int stage_area;        // bytes before the query buffer (stages, or the merge overlay)
 };
 
@@ -252,7 +256,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     const uint32_t qk_off = (uint32_t)(qk_box * kGroups) * gslot + (uint32_t)qk_t * 128u;
     const uint32_t qk_swz = (uint32_t)(qk_t & 7);
 
-    for (int k = w; k < n_stages; k += kConsumerWarps) {
+    const int nc = p.num_consumers;
+    for (int k = w; w < nc && k < n_stages; k += nc) {
       if (flags[0]) break;
       const int slot = k % NS;
       bool ok = mbar_wait_bounded(full0 + 8u * slot, (k / NS) & 1, p.err);
