@@ -1,0 +1,526 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = the whole hot path over one batch: the cache write of the step's
+new tokens (pa_reshape_and_cache through slot_mapping), any copy-on-write
+block copies, then paged decode attention (pa_decode: single pass, or
+split-KV partitions plus the log-sum-exp reduce).
+
+Default workload: the Qwen2-0.5B-shaped GQA batch (64 sequences, lengths
+U[128, 2048], 14 query / 2 KV heads of 64, block size 16, a pool of 16384
+blocks, 64 new tokens per step).  Other workloads: --workload.
+
+Printed: one JSON line (rank 0).  `value` is algorithmic GB/s of the whole
+step (bytes the step must move, divided by its device time); `roofline`
+reports the decode call alone against the measured HBM copy bandwidth;
+`e2e` repeats the step through the C ABI with host buffers (pinned H2D of
+the step's inputs, D2H of the output) inside the timed region;
+`cpu_baseline` times the CPU oracle on this host.  L2 is flushed (a 256 MB
+write) before every timed step.
+
+`--impl reference` times the CPU oracle as the reference arm, on the same
+workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak), µs per batch step"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+def make_workload(name: str):
+    if name == "qwen2_gqa":
+        return workloads.qwen2_gqa()
+    if name.startswith("opt13b_mha_bs"):
+        return workloads.opt13b_mha(block_size=int(name[len("opt13b_mha_bs"):]))
+    if name == "long_context":
+        return workloads.long_context(mixed=False)
+    if name == "long_context_mixed":
+        return workloads.long_context(mixed=True)
+    if name == "tiny":
+        return workloads.tiny()
+    raise SystemExit("unknown workload %s" % name)
+
+
+def step_bytes(case) -> dict:
+    """Algorithmic bytes of one step: what the operations must read and write once."""
+    eb = workloads.elem_bytes(case.dtype)
+    s, hq, hkv, d = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_size
+    lens = case.seq_lens.astype(np.int64)
+    blocks = int(((lens + case.block_size - 1) // case.block_size).sum())
+    decode = case.kv_bytes() + 2 * s * hq * d * eb + 4 * blocks + 4 * s
+    t = int((lens > 0).sum())  # one new token per sequence
+    write = t * hkv * d * eb * 2 * 2 + 8 * t  # read new K/V, write them, read slots
+    return {"decode": int(decode), "write": int(write), "step": int(decode + write)}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_cache_78_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("decode") or f in ("pa_device.cuh",):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, when it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = data.get(workload)
+    if not entry or entry.get("kernel_digest") != kernel_source_digest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [p for t, p in self.samples if t0 <= t <= t1] or [p for _, p in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def bf16_or_f32_to_device(torch, a, device):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class GpuStep:
+    """A workload resident on the device, and its step through the C ABI."""
+
+    def __init__(self, torch, pa, case, device, partition):
+        self.torch, self.pa, self.case, self.device = torch, pa, case, device
+        to_dev = lambda a: bf16_or_f32_to_device(torch, a, device)
+        self.cache = to_dev(case.initial_cache())
+        bt_host = torch.from_numpy(case.block_tables)
+        seqs, pos, rows = case.token_positions(exclude_last=True)
+        chunk = 1 << 16
+        for i in range(0, rows.size, chunk):  # prefill, through the library's own write
+            sl = slice(i, i + chunk)
+            slots = pa.pa_slot_mapping(bt_host, case.block_size, case.num_blocks,
+                                       torch.from_numpy(seqs[sl]), torch.from_numpy(pos[sl]))
+            pa.pa_reshape_and_cache(self.cache, to_dev(case.keys[rows[sl]]),
+                                    to_dev(case.values[rows[sl]]), slots.to(device))
+        seqs, pos, rows = case.token_positions(last_only=True)
+        self.slots_host = pa.pa_slot_mapping(bt_host, case.block_size, case.num_blocks,
+                                             torch.from_numpy(seqs), torch.from_numpy(pos))
+        self.k_host = case.keys[rows]
+        self.v_host = case.values[rows]
+        self.slots = self.slots_host.to(device)
+        self.k = to_dev(self.k_host)
+        self.v = to_dev(self.v_host)
+        self.q = to_dev(case.query)
+        self.bt = to_dev(case.block_tables)
+        self.sl = to_dev(case.seq_lens)
+        self.out = torch.empty_like(self.q)
+        self.partition = pa.pa_decode_partition_size(self.cache, case.num_seqs, case.num_heads,
+                                                     case.max_seq_len, partition)
+        nbytes = pa.pa_decode_workspace_size(self.cache, case.num_seqs, case.num_heads,
+                                             case.max_seq_len, self.partition)
+        self.ws = pa.alloc_workspace(nbytes, device)
+        self.launches = 2 + (1 if self.partition > 0 else 0)
+
+    def write(self):
+        self.pa.pa_reshape_and_cache(self.cache, self.k, self.v, self.slots)
+
+    def decode(self):
+        c = self.case
+        self.pa.pa_decode(self.out, self.q, self.cache, self.bt, self.sl, c.scale, c.max_seq_len,
+                          self.partition, self.ws)
+
+
+def run_gpu(args, rank, world, device):
+    import torch
+
+    import paged_kv_cache_78_gb300 as pa
+
+    torch.cuda.set_device(device)
+    case = make_workload(args.workload)
+    st = GpuStep(torch, pa, case, device, args.partition)
+    nbytes = step_bytes(case)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    graphs = None
+    if args.graph:
+        st.write()
+        st.decode()
+        torch.cuda.synchronize()
+        g_write, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_write):
+            st.write()
+        with torch.cuda.graph(g_decode):
+            st.decode()
+        graphs = (g_write, g_decode)
+
+    def write():
+        graphs[0].replay() if graphs else st.write()
+
+    def decode():
+        graphs[1].replay() if graphs else st.decode()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        write()
+        decode()
+    torch.cuda.synchronize()
+    flags = pa.pa_get_device_error()
+    if flags:
+        raise RuntimeError("device error word 0x%x after warm-up" % flags)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for e0, e1, e2 in ev:
+        flush.zero_()          # evict L2 between timed steps
+        e0.record(stream)
+        write()
+        e1.record(stream)
+        decode()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = sum(a.elapsed_time(c) for a, _, c in ev)
+    decode_ms = sum(b.elapsed_time(c) for _, b, c in ev)
+    flags = pa.pa_get_device_error()
+    if flags:
+        raise RuntimeError("device error word 0x%x after the timed region" % flags)
+
+    # End to end through the C ABI with host buffers: pinned H2D of the
+    # step's inputs, the step, D2H of the output, all inside the timed region.
+    host_in = {
+        "q": torch.from_numpy(np.ascontiguousarray(case.query).view(
+            np.int16 if case.dtype == "bf16" else np.float32)).pin_memory(),
+        "k": torch.from_numpy(np.ascontiguousarray(st.k_host).view(
+            np.int16 if case.dtype == "bf16" else np.float32)).pin_memory(),
+        "v": torch.from_numpy(np.ascontiguousarray(st.v_host).view(
+            np.int16 if case.dtype == "bf16" else np.float32)).pin_memory(),
+        "slots": st.slots_host.pin_memory(),
+        "bt": torch.from_numpy(case.block_tables).pin_memory(),
+        "sl": torch.from_numpy(case.seq_lens).pin_memory(),
+    }
+    dev_in = {"q": st.q, "k": st.k, "v": st.v, "slots": st.slots, "bt": st.bt, "sl": st.sl}
+    out_host = torch.empty(st.out.numel() * st.out.element_size(), dtype=torch.uint8).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = out_host.numel()
+
+    def e2e_step():
+        for key, h in host_in.items():
+            dev_in[key].view(h.dtype).copy_(h, non_blocking=True)
+        st.write()
+        st.decode()
+        out_host.copy_(st.out.view(torch.uint8).view(-1), non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(10, args.steps // 4)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(e2e_steps)]
+    for a, b in ev2:
+        flush.zero_()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2) / e2e_steps
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    if world > 1:
+        t = torch.tensor([step_ms, decode_ms, e2e_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, decode_ms, e2e_ms = t.tolist()
+    return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
+            "decode_ms": decode_ms / args.steps, "e2e_ms": e2e_ms, "clocks": clocks,
+            "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleStep:
+    """The step on the CPU oracle for the first `n` sequences of the batch."""
+
+    def __init__(self, case, n=None):
+        import oracle
+
+        self.oracle = oracle
+        self.case = case
+        n = case.num_seqs if n is None else n
+        self.n = n
+        self.cache = oracle.fill_cache(case, exclude_last=True)
+        seqs, pos, rows = case.token_positions(last_only=True)
+        keep = seqs < n
+        self.slots = oracle.slot_mapping(case.block_tables, seqs[keep], pos[keep], case.block_size)
+        self.k = np.ascontiguousarray(case.keys[rows[keep]])
+        self.v = np.ascontiguousarray(case.values[rows[keep]])
+        self.q = np.ascontiguousarray(case.query[:n])
+        self.bt = np.ascontiguousarray(case.block_tables[:n])
+        self.sl = np.ascontiguousarray(case.seq_lens[:n])
+
+    def run(self):
+        self.oracle.reshape_and_cache(self.cache, self.k, self.v, self.slots)
+        return self.oracle.decode(self.q, self.cache, self.bt, self.sl, self.case.scale)
+
+    def bytes(self):
+        sub = workloads.DecodeCase(**{**self.case.__dict__, "seq_lens": self.sl,
+                                      "block_tables": self.bt, "query": self.q})
+        return step_bytes(sub)["step"]
+
+
+def oracle_sample(case, per_step_s: float):
+    """An OracleStep over the longest prefix of sequences whose estimated
+    oracle time fits per_step_s (at least one sequence)."""
+    probe = OracleStep(case, 1)
+    probe.run()
+    t = time.perf_counter()
+    probe.run()
+    per_token = (time.perf_counter() - t) / max(1, int(case.seq_lens[0]))
+    cum = np.cumsum(case.seq_lens.astype(np.float64)) * per_token
+    n = int(max(1, np.searchsorted(cum, per_step_s, side="right")))
+    return probe if n == 1 else OracleStep(case, min(n, case.num_seqs))
+
+
+def time_oracle(case, budget_s: float, steps: int = 0):
+    """Median-free list of per-step times: `steps` runs, or as many as fit budget_s."""
+    per_step = budget_s / max(1, steps) if steps else budget_s / 5
+    step = oracle_sample(case, per_step)
+    times = []
+    t_start = time.time()
+    while (steps and len(times) < steps) or (not steps and (not times or time.time() - t_start < budget_s)):
+        t = time.perf_counter()
+        step.run()
+        times.append(time.perf_counter() - t)
+    return times, step, step.oracle.num_threads()
+
+
+def config_for(case, name):
+    lens = case.seq_lens
+    return {"workload": name, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+            "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
+            "block_size": case.block_size, "num_blocks": case.num_blocks,
+            "seq_len_min": int(lens.min()), "seq_len_max": int(lens.max()),
+            "seq_len_mean": round(float(lens.mean()), 1),
+            "new_tokens_per_step": int((lens > 0).sum()),
+            "bytes_per_step": step_bytes(case)["step"],
+            "l2": "flushed before every timed step (256 MB write)"}
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen2_gqa")
+    ap.add_argument("--partition", type=int, default=-1,
+                    help="tokens per split-KV partition; 0 = no split, -1 = library's choice")
+    ap.add_argument("--graph", type=int, default=1, help="replay the step as CUDA graphs")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        case = make_workload(args.workload)
+        total = args.steps + args.warmup
+        times, step, cores = time_oracle(case, budget_s=min(150.0, 2.0 * total), steps=total)
+        timed = times[args.warmup:]
+        sec = sum(timed) / len(timed)
+        value = step.bytes() / sec / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if case.dtype == "bf16" else "f32",
+                "data": "synthetic", "config": config_for(case, args.workload),
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                                 "kind": "oracle",
+                                 "sample": "per step: cache write of the new tokens and binary64 "
+                                           "decode of the first %d of %d sequences (%d bytes)"
+                                           % (step.n, case.num_seqs, step.bytes())},
+                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local_rank)
+    r = run_gpu(args, rank, world, device)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    case, st, nbytes = r["case"], r["step"], r["bytes"]
+    step_s = r["step_ms"] / 1e3
+    value = world * nbytes["step"] / step_s / 1e9
+    decode_gbs = nbytes["decode"] / (r["decode_ms"] / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    e2e_gbs = world * nbytes["step"] / (r["e2e_ms"] / 1e3) / 1e9
+
+    times, ostep, cores = time_oracle(case, budget_s=args.cpu_budget)
+    cpu_sec = statistics.median(times)
+    cpu_value = ostep.bytes() / cpu_sec / 1e9
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(r["step_ms"], 5),
+        "us_per_step": round(r["step_ms"] * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": config_for(case, args.workload),
+        "run": {"partition_size": st.partition, "cuda_graph": bool(args.graph),
+                "decode_bytes": nbytes["decode"],
+                "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gpu_launches": st.launches * args.steps,
+        "roofline": {
+            "kernel": "pa_decode (paged_decode_kernel%s)" % (" + lse_reduce_kernel" if st.partition else ""),
+            "bound": "hbm",
+            "achieved": round(decode_gbs, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(decode_gbs / peak, 4),
+            "us_per_launch": round(r["decode_ms"] * 1e3, 2),
+            "traffic": ncu_traffic(args.workload),
+        },
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "us_per_step": round(r["e2e_ms"] * 1e3, 2),
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "clocks": r["clocks"],
+        "cpu_baseline": {"value": round(cpu_value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": "cache write of the new tokens and binary64 decode of the "
+                                   "first %d of %d sequences, median of %d runs in %.0f s"
+                                   % (ostep.n, case.num_seqs, len(times), sum(times)),
+                         "ms_per_step": round(cpu_sec * 1e3, 2)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
