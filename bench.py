@@ -14,8 +14,9 @@ step (bytes the step must move, divided by its device time); `roofline`
 reports the decode call alone against the measured HBM copy bandwidth;
 `e2e` repeats the step through the C ABI with host buffers (pinned H2D of
 the step's inputs, D2H of the output) inside the timed region;
-`cpu_baseline` times the CPU oracle on this host.  L2 is flushed (a 256 MB
-write) before every timed step.
+`cpu_baseline` times the CPU oracle on this host.  L2 is flushed before every
+timed step: a 256 MB write, then a 256 MB read so that the written lines are
+evicted (and written back) before the step starts.
 
 `--impl reference` times the CPU oracle as the reference arm, on the same
 workload, metric and unit.
@@ -180,8 +181,9 @@ def bf16_or_f32_to_device(torch, a, device):
 class GpuStep:
     """A workload resident on the device, and its step through the C ABI."""
 
-    def __init__(self, torch, pa, case, device, partition):
+    def __init__(self, torch, pa, case, device, partition, kernel=0):
         self.torch, self.pa, self.case, self.device = torch, pa, case, device
+        self.kernel = kernel
         to_dev = lambda a: bf16_or_f32_to_device(torch, a, device)
         self.cache = to_dev(case.initial_cache())
         bt_host = torch.from_numpy(case.block_tables)
@@ -218,7 +220,7 @@ class GpuStep:
     def decode(self):
         c = self.case
         self.pa.pa_decode(self.out, self.q, self.cache, self.bt, self.sl, c.scale, c.max_seq_len,
-                          self.partition, self.ws)
+                          self.partition, self.ws, kernel=self.kernel)
 
 
 def run_gpu(args, rank, world, device):
@@ -228,10 +230,22 @@ def run_gpu(args, rank, world, device):
 
     torch.cuda.set_device(device)
     case = make_workload(args.workload)
-    st = GpuStep(torch, pa, case, device, args.partition)
+    st = GpuStep(torch, pa, case, device, args.partition, args.kernel)
     nbytes = step_bytes(case)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
+
+    class _Flush:
+        # Write a buffer larger than L2, then read another one: the read
+        # evicts the written lines (their write-back happens here, not in the
+        # timed step) and leaves L2 holding clean, unrelated data.
+        @staticmethod
+        def zero_():
+            flush_w.zero_()
+            flush_r.sum()
+
+    flush = _Flush
 
     graphs = None
     if args.graph:
@@ -312,6 +326,13 @@ def run_gpu(args, rank, world, device):
         st.decode()
         out_host.copy_(st.out.view(torch.uint8).view(-1), non_blocking=True)
 
+    if not args.e2e:
+        clocks = sampler.summary(t0, t1) if sampler else None
+        if sampler:
+            sampler.stop()
+        return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
+                "decode_ms": decode_ms / args.steps, "e2e_ms": None, "clocks": clocks,
+                "h2d": h2d, "d2h": d2h}
     for _ in range(max(3, args.warmup // 4)):
         flush.zero_()
         e2e_step()
@@ -408,7 +429,7 @@ def config_for(case, name):
             "seq_len_mean": round(float(lens.mean()), 1),
             "new_tokens_per_step": int((lens > 0).sum()),
             "bytes_per_step": step_bytes(case)["step"],
-            "l2": "flushed before every timed step (256 MB write)"}
+            "l2": "flushed before every timed step (256 MB write, then 256 MB read)"}
 
 
 # ---------------------------------------------------------------------------
@@ -423,8 +444,11 @@ def main():
     ap.add_argument("--partition", type=int, default=-1,
                     help="tokens per split-KV partition; 0 = no split, -1 = library's choice")
     ap.add_argument("--graph", type=int, default=1, help="replay the step as CUDA graphs")
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="decode kernel family: 0 = library's choice, 1 = CUDA cores, 2 = tensor cores")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
-                    help="seconds of oracle time for the CPU baseline")
+                    help="seconds of oracle time for the CPU baseline (0 = skip)")
+    ap.add_argument("--e2e", type=int, default=1, help="also time the step with host buffers")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
@@ -473,11 +497,22 @@ def main():
     value = world * nbytes["step"] / step_s / 1e9
     decode_gbs = nbytes["decode"] / (r["decode_ms"] / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
-    e2e_gbs = world * nbytes["step"] / (r["e2e_ms"] / 1e3) / 1e9
+    e2e = None
+    if r["e2e_ms"] is not None:
+        e2e = {"value": round(world * nbytes["step"] / (r["e2e_ms"] / 1e3) / 1e9, 2),
+               "unit": "GB/s", "us_per_step": round(r["e2e_ms"] * 1e3, 2),
+               "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
 
-    times, ostep, cores = time_oracle(case, budget_s=args.cpu_budget)
-    cpu_sec = statistics.median(times)
-    cpu_value = ostep.bytes() / cpu_sec / 1e9
+    cpu = None
+    if args.cpu_budget > 0:
+        times, ostep, cores = time_oracle(case, budget_s=args.cpu_budget)
+        cpu_sec = statistics.median(times)
+        cpu = {"value": round(ostep.bytes() / cpu_sec / 1e9, 4), "unit": "GB/s", "cores": cores,
+               "kind": "oracle",
+               "sample": "cache write of the new tokens and binary64 decode of the first %d of "
+                         "%d sequences, median of %d runs in %.0f s"
+                         % (ostep.n, case.num_seqs, len(times), sum(times)),
+               "ms_per_step": round(cpu_sec * 1e3, 2)}
 
     line = {
         "metric": METRIC,
@@ -495,6 +530,7 @@ def main():
         "data": "synthetic",
         "config": config_for(case, args.workload),
         "run": {"partition_size": st.partition, "cuda_graph": bool(args.graph),
+                "decode_kernel": {0: "auto", 1: "cuda cores", 2: "tensor cores"}[args.kernel],
                 "decode_bytes": nbytes["decode"],
                 "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": st.launches * args.steps,
@@ -509,15 +545,9 @@ def main():
             "us_per_launch": round(r["decode_ms"] * 1e3, 2),
             "traffic": ncu_traffic(args.workload),
         },
-        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "us_per_step": round(r["e2e_ms"] * 1e3, 2),
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "e2e": e2e,
         "clocks": r["clocks"],
-        "cpu_baseline": {"value": round(cpu_value, 4), "unit": "GB/s", "cores": cores,
-                         "kind": "oracle",
-                         "sample": "cache write of the new tokens and binary64 decode of the "
-                                   "first %d of %d sequences, median of %d runs in %.0f s"
-                                   % (ostep.n, case.num_seqs, len(times), sum(times)),
-                         "ms_per_step": round(cpu_sec * 1e3, 2)},
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
 

@@ -59,7 +59,7 @@ typedef enum pa_dtype { PA_BF16 = 0, PA_FP32 = 1 } pa_dtype;
 #define PA_DEVERR_SLOT 0x1u        /* reshape_and_cache: slot >= num_blocks * block_size */
 #define PA_DEVERR_BLOCK_ID 0x2u    /* decode / copy_blocks: block id outside [0, num_blocks) */
 #define PA_DEVERR_SEQ_LEN 0x4u     /* decode: seq_len > max_seq_len or > table capacity */
-#define PA_DEVERR_TIMEOUT 0x8u     /* a pipeline wait exceeded its limit (about 1 s) */
+#define PA_DEVERR_TIMEOUT 0x8u     /* a pipeline wait exceeded its limit (about 2 s) */
 
 /* Geometry of one layer's cache. */
 typedef struct pa_cache_desc {
@@ -135,9 +135,11 @@ pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* 
  *   workspace    device scratch of at least pa_decode_workspace_size() bytes,
  *                256-byte aligned; may be NULL when that size is 0.  Its
  *                contents need no initialisation and are clobbered.
- * G must be in 1..8.  Grouped heads share each K/V block load.
- * Arithmetic: fp32 dot products and an online fp32 softmax; bf16 output is
- * rounded to nearest even.  A sequence longer than max_seq_len or than its
+ * G = num_heads / num_kv_heads must be at most 16 for bf16 caches whose
+ * head size is 64 or 128 and whose blocks hold 8 tokens or more (tensor-core
+ * kernel), at most 8 otherwise (CUDA-core kernel).  Grouped heads share each
+ * K/V block load.  Arithmetic: fp32 scores and an online fp32 softmax; bf16
+ * output is rounded to nearest even.  A sequence longer than max_seq_len or than its
  * table row is recorded as PA_DEVERR_SEQ_LEN and its row is left undefined.
  * ------------------------------------------------------------------------- */
 pa_status pa_decode(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
@@ -145,6 +147,24 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
                     const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
                     int32_t max_seq_len, int32_t partition_size, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/* Kernel families for pa_decode_ex. */
+typedef enum pa_decode_kernel {
+  PA_KERNEL_AUTO = 0,   /* tensor cores where supported, else CUDA cores */
+  PA_KERNEL_SIMT = 1,   /* CUDA cores: fp32 dot products and accumulation; group <= 8 */
+  PA_KERNEL_TENSOR = 2  /* 5th-generation tensor cores: bf16 only, head size 64 or 128,
+                           group <= 16, block_size >= 8; scores and P.V accumulate in fp32,
+                           the softmax weights P enter the P.V product rounded to bf16 */
+} pa_decode_kernel;
+
+/* pa_decode with an explicit kernel family (PA_ERR_UNSUPPORTED when the
+ * requested family has no kernel for the arguments).  pa_decode is
+ * pa_decode_ex with PA_KERNEL_AUTO. */
+pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
+                       int32_t max_seq_len, int32_t partition_size, void* workspace,
+                       size_t workspace_bytes, int32_t kernel, void* stream);
 
 /* The partition size pa_decode uses for these arguments (0 = no split). */
 pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,

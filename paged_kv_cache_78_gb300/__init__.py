@@ -29,6 +29,9 @@ PA_ERR_DEVICE_CHECK = 6
 PA_ERR_TIMEOUT = 7
 PA_BF16 = 0
 PA_FP32 = 1
+PA_KERNEL_AUTO = 0
+PA_KERNEL_SIMT = 1
+PA_KERNEL_TENSOR = 2
 PA_DEVERR_SLOT = 0x1
 PA_DEVERR_BLOCK_ID = 0x2
 PA_DEVERR_SEQ_LEN = 0x4
@@ -36,7 +39,7 @@ PA_DEVERR_TIMEOUT = 0x8
 
 # Every function include/pa.h declares.
 EXPORTS = (
-    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_partition_size",
+    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_partition_size",
     "pa_decode_workspace_size", "pa_slot_mapping", "pa_pool_create", "pa_pool_destroy",
     "pa_pool_add_seq", "pa_pool_fork", "pa_pool_append_token", "pa_pool_append_tokens",
     "pa_pool_free_seq", "pa_pool_block_table", "pa_pool_fill_tables", "pa_pool_slot",
@@ -74,6 +77,7 @@ def _load() -> ctypes.CDLL:
         "pa_reshape_and_cache": [vp, desc, vp, vp, vp, i32, vp],
         "pa_copy_blocks": [vp, desc, vp, i32, vp],
         "pa_decode": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, vp],
+        "pa_decode_ex": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, i32, vp],
         "pa_decode_partition_size": [desc, i32, i32, i32, i32, p_i32],
         "pa_decode_workspace_size": [desc, i32, i32, i32, i32, p_sz],
         "pa_slot_mapping": [vp, i32, i32, i32, i32, vp, vp, i32, vp],
@@ -226,8 +230,9 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
 def pa_decode(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
               block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
               max_seq_len: int, partition_size: int = -1, workspace: torch.Tensor | None = None,
-              stream=None) -> None:
-    """out[s, hq] = softmax(scale * q[s, hq] . K_s) V_s over the paged tokens."""
+              stream=None, kernel: int = PA_KERNEL_AUTO) -> None:
+    """out[s, hq] = softmax(scale * q[s, hq] . K_s) V_s over the paged tokens.
+    kernel: PA_KERNEL_AUTO, PA_KERNEL_SIMT or PA_KERNEL_TENSOR (pa_decode_ex)."""
     desc = cache_desc(cache)
     s, hq, d = query.shape
     if out.shape != query.shape or d != desc.head_size:
@@ -239,12 +244,12 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
-    _check(lib.pa_decode(_dev_ptr(out, "out"), _dev_ptr(query, "query"),
-                         _dev_ptr(cache, "cache"), ctypes.byref(desc),
-                         _dev_ptr(block_tables, "block_tables", torch.int32),
-                         block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens", torch.int32), s, hq,
-                         float(scale), int(max_seq_len), int(partition_size), ws_ptr, ws_bytes,
-                         _stream(stream)), "pa_decode")
+    _check(lib.pa_decode_ex(_dev_ptr(out, "out"), _dev_ptr(query, "query"),
+                            _dev_ptr(cache, "cache"), ctypes.byref(desc),
+                            _dev_ptr(block_tables, "block_tables", torch.int32),
+                            block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens", torch.int32), s,
+                            hq, float(scale), int(max_seq_len), int(partition_size), ws_ptr,
+                            ws_bytes, int(kernel), _stream(stream)), "pa_decode")
 
 
 def pa_slot_mapping(block_tables: torch.Tensor, block_size: int, num_blocks: int,
@@ -363,3 +368,10 @@ class Pool:
 
     def num_free(self) -> int:
         return int(lib.pa_pool_num_free(self._h))
+
+
+def tensor_core_supported(cache: torch.Tensor, num_heads: int) -> bool:
+    """Whether PA_KERNEL_TENSOR has a kernel for this cache and head count."""
+    d = cache_desc(cache)
+    g = num_heads // d.num_kv_heads
+    return d.dtype == PA_BF16 and d.head_size in (64, 128) and g <= 16 and d.block_size >= 8

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "decode_kernel.cuh"
+#include "decode_tc_kernel.cuh"
 #include "pa.h"
 #include "pa_launch.h"
 
@@ -229,10 +230,22 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
                     const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
                     int32_t max_seq_len, int32_t partition_size, void* workspace,
                     size_t workspace_bytes, void* stream) {
+  return pa_decode_ex(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens,
+                      num_seqs, num_heads, scale, max_seq_len, partition_size, workspace,
+                      workspace_bytes, PA_KERNEL_AUTO, stream);
+}
+
+pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
+                       int32_t max_seq_len, int32_t partition_size, void* workspace,
+                       size_t workspace_bytes, int32_t kernel, void* stream) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || num_heads < 1 || max_seq_len < 0 ||
       max_blocks_per_seq < 1 || !std::isfinite(scale))
+    return PA_ERR_INVALID_ARG;
+  if (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_SIMT && kernel != PA_KERNEL_TENSOR)
     return PA_ERR_INVALID_ARG;
   if (num_heads % desc->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
@@ -242,8 +255,23 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return PA_ERR_INVALID_ARG;
   const int group = num_heads / desc->num_kv_heads;
-  if (!head_size_supported(desc->head_size) || group > 8) return PA_ERR_UNSUPPORTED;
-  if (desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  const int D = desc->head_size;
+  const int BS = desc->block_size;
+  if (!head_size_supported(D) || desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  // Tensor cores: bf16, head size 64 or 128, query group up to 16, blocks of
+  // at least 8 tokens (a TMA box then fills whole 1024-byte swizzle atoms).
+  const bool tc_ok = desc->dtype == PA_BF16 && (D == 64 || D == 128) && group <= pa::kTcHeads &&
+                     BS >= 8;
+  bool use_tc;
+  if (kernel == PA_KERNEL_TENSOR) {
+    if (!tc_ok) return PA_ERR_UNSUPPORTED;
+    use_tc = true;
+  } else if (kernel == PA_KERNEL_SIMT) {
+    use_tc = false;
+  } else {
+    use_tc = tc_ok;
+  }
+  if (!use_tc && group > 8) return PA_ERR_UNSUPPORTED;
 
   unsigned int* err = nullptr;
   int sms = 0;
@@ -255,49 +283,64 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
   float* part_o = nullptr;
   float* part_lse = nullptr;
   if (part > 0) {
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, desc->head_size, max_parts);
+    const size_t need = workspace_bytes_for(num_seqs, num_heads, D, max_parts);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
       return PA_ERR_INVALID_ARG;
     part_o = static_cast<float*>(workspace);
-    size_t o_bytes = (size_t)num_seqs * num_heads * max_parts * desc->head_size * 4;
+    size_t o_bytes = (size_t)num_seqs * num_heads * max_parts * D * 4;
     o_bytes = (o_bytes + 255) / 256 * 256;
     part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   }
 
-  // Stage geometry: 32 tokens per stage, TMA boxes of min(block_size, 32)
-  // rows, one box per 128-byte column group, each box at a 1024-byte
-  // aligned slot so the 128-byte swizzle pattern starts on an atom.
-  const int D = desc->head_size;
-  const int BS = desc->block_size;
-  const int R = BS < pa::kStageTokens ? BS : pa::kStageTokens;
-  const int groups = D * es / 128;
-  const int gslot = R * 128 > 1024 ? R * 128 : 1024;
-  const int region = (pa::kStageTokens / R) * groups * gslot;
-  const int stage_bytes = 2 * region;
-  // As many stages as the budget holds (at most 64); at least two when two
-  // fit in a CTA's shared memory, else one (tiny blocks of long fp32 rows).
-  const int merge = pa::decode_merge_bytes(group, D);
-  auto area_for = [&](int n) {
-    const int a = n * stage_bytes;
-    return a < merge ? (merge + 15) / 16 * 16 : a;
-  };
-  // Every ring slot belongs to one consumer warp, so the stage count is a
-  // multiple of the consumer count: 4 consumers with 4, 8, ... stages, or
-  // 1-3 consumers with as many stages when fewer fit.
-  int ns = kStageBudgetBytes / stage_bytes;
-  if (ns > 64) ns = 64;
-  if (ns < 2) ns = pa::decode_smem_bytes(area_for(2), group, D) <= kMaxSmemPerCta ? 2 : 1;
-  if (ns >= pa::kConsumerWarps) ns -= ns % pa::kConsumerWarps;
-  const int consumers = ns < pa::kConsumerWarps ? ns : pa::kConsumerWarps;
-  const int stage_area = area_for(ns);
-  const int smem = pa::decode_smem_bytes(stage_area, group, D);
+  pa::DecodeParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  int R, smem;
+  if (use_tc) {
+    // 128-token stages; a box is min(block_size, 128) rows of one 128-byte
+    // column group.  Three stages.
+    R = BS < pa::kTcTokens ? BS : pa::kTcTokens;
+    prm.num_stages = 3;
+    prm.num_consumers = 1;
+    smem = pa::tc_smem_layout(D, prm.num_stages).total;
+  } else {
+    // 32-token stages, TMA boxes of min(block_size, 32) rows, one box per
+    // 128-byte column group, each box at a 1024-byte aligned slot so the
+    // 128-byte swizzle pattern starts on an atom.
+    R = BS < pa::kStageTokens ? BS : pa::kStageTokens;
+    const int groups = D * es / 128;
+    const int gslot = R * 128 > 1024 ? R * 128 : 1024;
+    const int region = (pa::kStageTokens / R) * groups * gslot;
+    const int stage_bytes = 2 * region;
+    // As many stages as the budget holds (at most 64); at least two when two
+    // fit in a CTA's shared memory, else one.  Every ring slot belongs to one
+    // consumer warp, so the stage count is a multiple of the consumer count:
+    // 4 consumers with 4, 8, ... stages, or 1-3 consumers with as many stages.
+    const int merge = pa::decode_merge_bytes(group, D);
+    auto area_for = [&](int n) {
+      const int a = n * stage_bytes;
+      return a < merge ? (merge + 15) / 16 * 16 : a;
+    };
+    int ns = kStageBudgetBytes / stage_bytes;
+    if (ns > 64) ns = 64;
+    if (ns < 2) ns = pa::decode_smem_bytes(area_for(2), group, D) <= kMaxSmemPerCta ? 2 : 1;
+    if (ns >= pa::kConsumerWarps) ns -= ns % pa::kConsumerWarps;
+    prm.num_stages = ns;
+    prm.num_consumers = ns < pa::kConsumerWarps ? ns : pa::kConsumerWarps;
+    prm.group_slot = gslot;
+    prm.region_bytes = region;
+    prm.stage_area = area_for(ns);
+    smem = pa::decode_smem_bytes(prm.stage_area, group, D);
+  }
   if (smem > kMaxSmemPerCta) return PA_ERR_UNSUPPORTED;
 
   EncodeTiledFn encode = nullptr;
   if ((st = encode_fn(&encode)) != PA_OK) return st;
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
+  // The pool as a 5-D tensor (innermost first): 128-byte column chunk,
+  // column group, KV head, token within block, (K or V) * num_blocks + block.
   const int inner = 128 / es;
+  const int groups = D * es / 128;
   const cuuint64_t gdim[5] = {(cuuint64_t)inner, (cuuint64_t)groups,
                               (cuuint64_t)desc->num_kv_heads, (cuuint64_t)BS,
                               2ull * (cuuint64_t)desc->num_blocks};
@@ -314,7 +357,6 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return PA_ERR_CUDA;
 
-  pa::DecodeParams prm;
   prm.out = out;
   prm.query = query;
   prm.block_tables = block_tables;
@@ -327,24 +369,24 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
   prm.log2_block_size = ilog2(BS);
   prm.num_kv_heads = desc->num_kv_heads;
   prm.num_heads = num_heads;
+  prm.group = group;
   prm.max_blocks_per_seq = max_blocks_per_seq;
   prm.partition_tokens = part;
   prm.max_parts = max_parts;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm.box_rows = R;
   prm.log2_box_rows = ilog2(R);
-  prm.group_slot = gslot;
-  prm.region_bytes = region;
-  prm.num_stages = ns;
-  prm.num_consumers = consumers;
-  prm.stage_area = stage_area;
 
   const dim3 grid((unsigned)max_parts, (unsigned)desc->num_kv_heads, (unsigned)num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool supported = true;
-  cudaError_t e = desc->dtype == PA_BF16
-                      ? pa::launch_decode_bf16(D, group, grid, smem, s, map, prm, &supported)
-                      : pa::launch_decode_f32(D, group, grid, smem, s, map, prm, &supported);
+  cudaError_t e;
+  if (use_tc)
+    e = pa::launch_decode_tc(D, grid, smem, s, map, prm, &supported);
+  else if (desc->dtype == PA_BF16)
+    e = pa::launch_decode_bf16(D, group, grid, smem, s, map, prm, &supported);
+  else
+    e = pa::launch_decode_f32(D, group, grid, smem, s, map, prm, &supported);
   if (!supported) return PA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (part > 0) {

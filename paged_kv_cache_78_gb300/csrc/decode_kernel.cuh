@@ -54,12 +54,13 @@ struct DecodeParams {
   int log2_block_size;
   int num_kv_heads;
   int num_heads;
+  int group;             // query heads per KV head
   int max_blocks_per_seq;
   int partition_tokens;  // 0 = the whole sequence in one CTA
   int max_parts;         // grid.x in split mode
   float scale_log2;      // scale * log2(e)
   // shared-memory geometry, bytes
-  int box_rows;          // tokens per TMA box: min(block_size, 32)
+  int box_rows;          // tokens per TMA box: min(block_size, tokens per stage)
   int log2_box_rows;
   int group_slot;        // bytes per (box, 128-byte column group): max(box_rows*128, 1024)
   int region_bytes;      // K (or V) part of one stage

@@ -11,9 +11,11 @@
 
 namespace pa {
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer
-// (about one second), records PA_DEVERR_TIMEOUT and lets the kernel return.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// A bounded wait gives up after this many SM clock cycles (about two seconds
+// at 2 GHz), records PA_DEVERR_TIMEOUT and lets the kernel return.  The
+// clock is read only every 64 polls, so a wait that succeeds quickly costs
+// nothing beyond the polls.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ void record_error(unsigned int* err, unsigned int bits) {
   if (err) atomicOr(err, bits);
@@ -21,12 +23,6 @@ __device__ __forceinline__ void record_error(unsigned int* err, unsigned int bit
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ---- mbarrier -------------------------------------------------------------
@@ -61,14 +57,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and records PA_DEVERR_TIMEOUT) if that takes longer than kWaitLimitNs.
+// (and records PA_DEVERR_TIMEOUT) if that takes longer than kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 63u) == 0 && clock64() - t0 > kWaitLimitCycles) {
       record_error(err, PA_DEVERR_TIMEOUT);
       return false;
     }

@@ -78,7 +78,7 @@ class DeviceCase:
         self.step_keys = to_device(case.keys[rows], device)
         self.step_values = to_device(case.values[rows], device)
 
-    def step(self, partition_size=-1, workspace=None):
+    def step(self, partition_size=-1, workspace=None, kernel=pa.PA_KERNEL_AUTO):
         c = self.case
         pa.pa_reshape_and_cache(self.cache, self.step_keys, self.step_values, self.step_slots)
         if workspace is None:
@@ -86,7 +86,7 @@ class DeviceCase:
                                                  c.max_seq_len, partition_size)
             workspace = pa.alloc_workspace(nbytes, self.device)
         pa.pa_decode(self.out, self.query, self.cache, self.block_tables, self.seq_lens,
-                     c.scale, c.max_seq_len, partition_size, workspace)
+                     c.scale, c.max_seq_len, partition_size, workspace, kernel=kernel)
         return self.out
 
 

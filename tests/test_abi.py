@@ -65,7 +65,9 @@ def test_decode_argument_checks():
     assert call(mb=0) == pa.PA_ERR_INVALID_ARG
     assert call(s=0) == pa.PA_OK                           # empty batch: no-op
     assert call(desc=desc(head_size=96)) == pa.PA_ERR_UNSUPPORTED
-    assert call(hq=2 * 9) == pa.PA_ERR_UNSUPPORTED         # group of 9
+    assert call(hq=2 * 17) == pa.PA_ERR_UNSUPPORTED        # group of 17
+    assert call(hq=2 * 9, desc=desc(dtype=pa.PA_FP32)) == pa.PA_ERR_UNSUPPORTED  # fp32, group 9
+    assert call(hq=2 * 9, desc=desc(block_size=4)) == pa.PA_ERR_UNSUPPORTED     # 4-token blocks
 
 
 def test_partition_and_workspace_sizes():

@@ -24,15 +24,25 @@ def clean_error_word():
     yield
 
 
+def kernels_for(case):
+    """CUDA-core kernel always; tensor-core kernel where it applies."""
+    tc = (case.dtype == "bf16" and case.head_size in (64, 128) and case.block_size >= 8
+          and case.num_heads // case.num_kv_heads <= 16)
+    simt = case.num_heads // case.num_kv_heads <= 8
+    return ([pa.PA_KERNEL_SIMT] if simt else []) + ([pa.PA_KERNEL_TENSOR] if tc else [])
+
+
 def check(case, partitions=(0, -1)):
     ref, cache_ref = oracle_reference(case)
-    for p in partitions:
-        dc = DeviceCase(case)
-        out = dc.step(p)
-        torch.cuda.synchronize()
-        assert pa.pa_get_device_error() == 0
-        assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
-        assert_close(to_f64(out), ref, case.dtype, "%s partition=%s" % (case.name, p))
+    for kernel in kernels_for(case):
+        for p in partitions:
+            dc = DeviceCase(case)
+            out = dc.step(p, kernel=kernel)
+            torch.cuda.synchronize()
+            assert pa.pa_get_device_error() == 0
+            assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
+            assert_close(to_f64(out), ref, case.dtype,
+                         "%s kernel=%d partition=%s" % (case.name, kernel, p))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
@@ -58,6 +68,12 @@ SHAPES = [
     (12, 2, 256, 16, [150, 33], "bf16", (0, 32)),
     (40, 40, 128, 16, [1, 2048], "bf16", (0, 512)),
     (16, 2, 64, 16, [5000], "bf16", (32, 256)),
+    # tensor-core kernel specifics: groups up to 16, stage (128-token) edges,
+    # boxes of 128 rows (block size 256), 8-token blocks
+    (32, 2, 64, 16, [1, 127, 128, 129, 255, 256, 257, 1000], "bf16", (0, 128, 384)),
+    (24, 2, 128, 8, [8, 9, 300, 777], "bf16", (0, 256)),
+    (16, 16, 128, 256, [100, 256, 700], "bf16", (0, 512)),
+    (12, 1, 64, 32, [2, 4096], "bf16", (0, 640)),
 ]
 
 
@@ -70,22 +86,34 @@ def test_decode_shapes(hq, hkv, d, bs, lens, dtype, parts):
     check(case, partitions=parts)
 
 
-def test_block_relabelling_gives_identical_output():
+@pytest.mark.parametrize("kernel", [pa.PA_KERNEL_SIMT, pa.PA_KERNEL_TENSOR])
+def test_block_relabelling_gives_identical_output(kernel):
     case = workloads.custom(3, 8, 2, 128, 16, [70, 300, 33], "bf16", seed=3)
-    a = DeviceCase(case).step(0).clone()
+    a = DeviceCase(case).step(0, kernel=kernel).clone()
     perm = np.random.default_rng(2).permutation(case.num_blocks)
     case2 = workloads.custom(3, 8, 2, 128, 16, [70, 300, 33], "bf16", seed=3)
     case2.block_tables = perm[case.block_tables].astype(np.int32)
-    b = DeviceCase(case2).step(0)
+    b = DeviceCase(case2).step(0, kernel=kernel)
     assert torch.equal(a, b)
 
 
-def test_repeated_calls_are_deterministic():
+@pytest.mark.parametrize("kernel", [pa.PA_KERNEL_SIMT, pa.PA_KERNEL_TENSOR])
+def test_repeated_calls_are_deterministic(kernel):
     case = workloads.custom(4, 14, 2, 64, 16, [100, 900, 2000, 1], "bf16", seed=8)
     dc = DeviceCase(case)
-    a = dc.step(128).clone()
-    b = dc.step(128).clone()
+    a = dc.step(128, kernel=kernel).clone()
+    b = dc.step(128, kernel=kernel).clone()
     assert torch.equal(a, b)
+
+
+def test_tensor_kernel_rejects_shapes_it_has_no_kernel_for():
+    for args in [(4, 4, 64, 4, [9, 9], "bf16"),     # block size below 8
+                 (4, 4, 64, 16, [9, 9], "fp32"),    # fp32
+                 (4, 4, 256, 16, [9, 9], "bf16")]:  # head size 256
+        case = workloads.custom(2, *args[:4], args[4], args[5], seed=1)
+        dc = DeviceCase(case)
+        with pytest.raises(pa.PAError):
+            dc.step(0, kernel=pa.PA_KERNEL_TENSOR)
 
 
 def test_bad_block_id_is_recorded_and_reads_zeros():
