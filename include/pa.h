@@ -150,7 +150,7 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
 
 /* Kernel families for pa_decode_ex. */
 typedef enum pa_decode_kernel {
-  PA_KERNEL_AUTO = 0,   /* tensor cores where supported, else CUDA cores */
+  PA_KERNEL_AUTO = 0,   /* CUDA cores for groups up to 8, tensor cores for groups of 9..16 */
   PA_KERNEL_SIMT = 1,   /* CUDA cores: fp32 dot products and accumulation; group <= 8 */
   PA_KERNEL_TENSOR = 2  /* 5th-generation tensor cores: bf16 only, head size 64 or 128,
                            group <= 16, block_size >= 8; scores and P.V accumulate in fp32,

@@ -269,7 +269,10 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   } else if (kernel == PA_KERNEL_SIMT) {
     use_tc = false;
   } else {
-    use_tc = tc_ok;
+    // Automatic choice: the tensor-core kernel where only it applies (groups
+    // of 9..16); elsewhere the CUDA-core kernel, which measures faster on the
+    // benchmark workloads in its present one-CTA-per-partition form.
+    use_tc = tc_ok && group > 8;
   }
   if (!use_tc && group > 8) return PA_ERR_UNSUPPORTED;
 
