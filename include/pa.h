@@ -178,6 +178,35 @@ pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t partition_size, size_t* bytes);
 
 /* ---------------------------------------------------------------------------
+ * pa_decode without a caller-provided workspace.  The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate
+ * device memory — an engine that reserves all device memory for its block
+ * pool at start-up and forbids later allocations, or a plain C caller with no
+ * caching allocator, for whom cudaMalloc/cudaFree around each decode step
+ * would synchronise the device.
+ *
+ * Same arguments and result as pa_decode with the workspace left out: the
+ * split-KV partials go to an array the library keeps in device memory, of
+ * PA_NO_ALLOC_WORKSPACE_BYTES (16 MiB) per device, held until the process
+ * exits.  A call whose partials need more (pa_decode_workspace_size) returns
+ * PA_ERR_INVALID_ARG and launches nothing; so does every argument pa_decode
+ * rejects.  The call allocates nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (nothing in it needs to start at zero).  Calls whose
+ *     work overlaps on the GPU (two streams, or two threads) race on it:
+ *     order them on one stream, or use pa_decode with separate workspaces.
+ * ------------------------------------------------------------------------- */
+#define PA_NO_ALLOC_WORKSPACE_BYTES (16u << 20)
+pa_status pa_decode_no_alloc(void* out, const void* query, const void* cache,
+                             const pa_cache_desc* desc, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                             int32_t num_seqs, int32_t num_heads, float scale,
+                             int32_t max_seq_len, int32_t partition_size, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Slot mapping from block tables (host).  slots[i] is the physical slot of
  * token positions[i] of sequence seq_idx[i]:
  *   table[seq][pos / block_size] * block_size + pos % block_size

@@ -39,7 +39,8 @@ PA_DEVERR_TIMEOUT = 0x8
 
 # Every function include/pa.h declares.
 EXPORTS = (
-    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_partition_size",
+    "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_no_alloc",
+    "pa_decode_partition_size",
     "pa_decode_workspace_size", "pa_slot_mapping", "pa_pool_create", "pa_pool_destroy",
     "pa_pool_add_seq", "pa_pool_fork", "pa_pool_append_token", "pa_pool_append_tokens",
     "pa_pool_free_seq", "pa_pool_block_table", "pa_pool_fill_tables", "pa_pool_slot",
@@ -78,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "pa_copy_blocks": [vp, desc, vp, i32, vp],
         "pa_decode": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, vp],
         "pa_decode_ex": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, i32, vp],
+        "pa_decode_no_alloc": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp],
         "pa_decode_partition_size": [desc, i32, i32, i32, i32, p_i32],
         "pa_decode_workspace_size": [desc, i32, i32, i32, i32, p_sz],
         "pa_slot_mapping": [vp, i32, i32, i32, i32, vp, vp, i32, vp],
@@ -250,6 +252,29 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
                             block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens", torch.int32), s,
                             hq, float(scale), int(max_seq_len), int(partition_size), ws_ptr,
                             ws_bytes, int(kernel), _stream(stream)), "pa_decode")
+
+
+NO_ALLOC_WORKSPACE_BYTES = 16 << 20
+
+
+def pa_decode_no_alloc(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
+                       block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                       max_seq_len: int, partition_size: int = -1, stream=None) -> None:
+    """pa_decode with the split-KV scratch in the library's own device array
+    (for callers that cannot allocate device memory; see include/pa.h)."""
+    desc = cache_desc(cache)
+    s, hq, d = query.shape
+    if out.shape != query.shape or d != desc.head_size:
+        raise ValueError("query/out must be [num_seqs, num_heads, head_size]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != s or seq_lens.shape != (s,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks], seq_lens [num_seqs]")
+    _check(lib.pa_decode_no_alloc(_dev_ptr(out, "out"), _dev_ptr(query, "query"),
+                                  _dev_ptr(cache, "cache"), ctypes.byref(desc),
+                                  _dev_ptr(block_tables, "block_tables", torch.int32),
+                                  block_tables.shape[1],
+                                  _dev_ptr(seq_lens, "seq_lens", torch.int32), s, hq,
+                                  float(scale), int(max_seq_len), int(partition_size),
+                                  _stream(stream)), "pa_decode_no_alloc")
 
 
 def pa_slot_mapping(block_tables: torch.Tensor, block_size: int, num_blocks: int,
