@@ -133,8 +133,13 @@ pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* 
  *                combined by a log-sum-exp reduce kernel.  -1: the library
  *                picks (pa_decode_partition_size reports the choice).
  *   workspace    device scratch of at least pa_decode_workspace_size() bytes,
- *                256-byte aligned; may be NULL when that size is 0.  Its
- *                contents need no initialisation and are clobbered.
+ *                256-byte aligned.  Its first 256 bytes hold the tensor-core
+ *                kernel's work counter: they must be zero when the workspace
+ *                is first used (allocate it zeroed), and every call leaves
+ *                them zero.  The rest (split-KV partials) needs no
+ *                initialisation.  It may be NULL for a CUDA-core call that
+ *                does not split.  Calls that overlap on the GPU need separate
+ *                workspaces.
  * G = num_heads / num_kv_heads must be at most 16 for bf16 caches whose
  * head size is 64 or 128 and whose blocks hold 8 tokens or more (tensor-core
  * kernel), at most 8 otherwise (CUDA-core kernel).  Grouped heads share each
@@ -171,8 +176,9 @@ pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t num_heads, int32_t max_seq_len,
                                    int32_t partition_size, int32_t* resolved);
 
-/* Workspace bytes pa_decode needs for these arguments (0 when it does not split):
- * num_seqs * num_heads * max_partitions * (head_size + 1) * 4, rounded up to 256. */
+/* Workspace bytes pa_decode needs for these arguments: a 256-byte header,
+ * plus num_seqs * num_heads * max_partitions * (head_size + 1) * 4 (each part
+ * rounded up to 256) when it splits. */
 pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t num_heads, int32_t max_seq_len,
                                    int32_t partition_size, size_t* bytes);
@@ -195,7 +201,8 @@ pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
  *   - Every call on a device shares the one array, which keeps the previous
- *     call's contents (nothing in it needs to start at zero).  Calls whose
+ *     call's contents; its work-counter header starts at zero and every call
+ *     leaves it zero, so nothing needs clearing between calls.  Calls whose
  *     work overlaps on the GPU (two streams, or two threads) race on it:
  *     order them on one stream, or use pa_decode with separate workspaces.
  * ------------------------------------------------------------------------- */

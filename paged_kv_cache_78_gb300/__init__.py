@@ -223,10 +223,11 @@ def pa_decode_workspace_size(cache_or_desc, num_seqs: int, num_heads: int, max_s
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
-    """Caller-owned decode workspace (256-byte aligned by the caching allocator)."""
+    """Caller-owned decode workspace: zeroed (its header must start at zero),
+    256-byte aligned by the caching allocator."""
     if nbytes == 0:
         return None
-    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
 def pa_decode(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,

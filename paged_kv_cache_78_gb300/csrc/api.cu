@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -114,12 +115,20 @@ pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int max_seq_le
   return PA_OK;
 }
 
-size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_parts) {
+// Workspace: a 256-byte header (the tensor-core kernel's work counter), then,
+// when splitting, the fp32 partial outputs and their log-sum-exp values.
+constexpr size_t kWorkspaceHeader = 256;
+
+size_t partial_o_bytes(int num_seqs, int num_heads, int head_size, int max_parts) {
   const size_t rows = (size_t)num_seqs * num_heads * max_parts;
-  size_t o_bytes = rows * head_size * 4;
-  o_bytes = (o_bytes + 255) / 256 * 256;
-  size_t lse_bytes = (rows * 4 + 255) / 256 * 256;
-  return o_bytes + lse_bytes;
+  return (rows * head_size * 4 + 255) / 256 * 256;
+}
+
+size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_parts) {
+  if (max_parts == 0) return kWorkspaceHeader;
+  const size_t rows = (size_t)num_seqs * num_heads * max_parts;
+  return kWorkspaceHeader + partial_o_bytes(num_seqs, num_heads, head_size, max_parts) +
+         (rows * 4 + 255) / 256 * 256;
 }
 
 }  // namespace
@@ -219,9 +228,8 @@ pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
   pa_status st = pa_decode_partition_size(desc, num_seqs, num_heads, max_seq_len,
                                           partition_size, &p);
   if (st != PA_OK) return st;
-  *bytes = p == 0 ? 0
-                  : workspace_bytes_for(num_seqs, num_heads, desc->head_size,
-                                        (max_seq_len + p - 1) / p);
+  *bytes = workspace_bytes_for(num_seqs, num_heads, desc->head_size,
+                               p == 0 ? 0 : (max_seq_len + p - 1) / p);
   return PA_OK;
 }
 
@@ -261,7 +269,7 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   // Tensor cores: bf16, head size 64 or 128, query group up to 16, blocks of
   // at least 8 tokens (a TMA box then fills whole 1024-byte swizzle atoms).
   const bool tc_ok = desc->dtype == PA_BF16 && (D == 64 || D == 128) && group <= pa::kTcHeads &&
-                     BS >= 8;
+                     BS >= 8 && aligned(query, 16) && (long long)num_seqs * num_heads < (1ll << 31);
   bool use_tc;
   if (kernel == PA_KERNEL_TENSOR) {
     if (!tc_ok) return PA_ERR_UNSUPPORTED;
@@ -285,14 +293,18 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   const int max_parts = part > 0 ? (max_seq_len + part - 1) / part : 1;
   float* part_o = nullptr;
   float* part_lse = nullptr;
-  if (part > 0) {
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, D, max_parts);
+  unsigned int* sched = nullptr;
+  if (part > 0 || use_tc) {
+    const size_t need = workspace_bytes_for(num_seqs, num_heads, D, part > 0 ? max_parts : 0);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
       return PA_ERR_INVALID_ARG;
-    part_o = static_cast<float*>(workspace);
-    size_t o_bytes = (size_t)num_seqs * num_heads * max_parts * D * 4;
-    o_bytes = (o_bytes + 255) / 256 * 256;
-    part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    sched = reinterpret_cast<unsigned int*>(ws);
+    if (part > 0) {
+      part_o = reinterpret_cast<float*>(ws + kWorkspaceHeader);
+      part_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader +
+                                          partial_o_bytes(num_seqs, num_heads, D, max_parts));
+    }
   }
 
   pa::DecodeParams prm;
@@ -305,6 +317,9 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
     prm.num_stages = 3;
     prm.num_consumers = 1;
     smem = pa::tc_smem_layout(D, prm.num_stages).total;
+    prm.sched = sched;
+    prm.total_items = (int)std::min<long long>((long long)num_seqs * desc->num_kv_heads * max_parts,
+                                               (1ll << 31) - 1);
   } else {
     // 32-token stages, TMA boxes of min(block_size, 32) rows, one box per
     // 128-byte column group, each box at a 1024-byte aligned slot so the
@@ -359,6 +374,21 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return PA_ERR_CUDA;
+  // The tensor-core kernel loads each work item's 16 query rows by TMA: the
+  // queries as [rows = num_seqs * num_heads][column group][64 elements].
+  CUtensorMap qmap;
+  std::memset(&qmap, 0, sizeof(qmap));
+  if (use_tc) {
+    const cuuint64_t qdim[3] = {64ull, (cuuint64_t)(D / 64),
+                                (cuuint64_t)num_seqs * (cuuint64_t)num_heads};
+    const cuuint64_t qstride[2] = {128ull, (cuuint64_t)D * 2};
+    const cuuint32_t qbox[3] = {64u, 1u, (cuuint32_t)pa::kTcHeads};
+    const cuuint32_t qes[3] = {1u, 1u, 1u};
+    cr = encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(query), qdim,
+                qstride, qbox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return PA_ERR_CUDA;
+  }
 
   prm.out = out;
   prm.query = query;
@@ -372,6 +402,7 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   prm.log2_block_size = ilog2(BS);
   prm.num_kv_heads = desc->num_kv_heads;
   prm.num_heads = num_heads;
+  prm.num_seqs = num_seqs;
   prm.group = group;
   prm.max_blocks_per_seq = max_blocks_per_seq;
   prm.partition_tokens = part;
@@ -385,7 +416,7 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   bool supported = true;
   cudaError_t e;
   if (use_tc)
-    e = pa::launch_decode_tc(D, grid, smem, s, map, prm, &supported);
+    e = pa::launch_decode_tc(D, sms, smem, s, map, qmap, prm, &supported);
   else if (desc->dtype == PA_BF16)
     e = pa::launch_decode_bf16(D, group, grid, smem, s, map, prm, &supported);
   else

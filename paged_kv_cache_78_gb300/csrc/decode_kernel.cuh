@@ -49,6 +49,9 @@ struct DecodeParams {
   float* part_o;                // [S][Hq][max_parts][D]: normalised partial outputs
   float* part_lse;              // [S][Hq][max_parts]: log2-domain log-sum-exp of each partial
   unsigned int* err;            // device error word
+  unsigned int* sched;          // tensor-core kernel: [0] next work item, [1] CTAs finished
+  int total_items;              // tensor-core kernel: num_seqs * num_kv_heads * max_parts
+  int num_seqs;
   int num_blocks;
   int block_size;
   int log2_block_size;

@@ -54,8 +54,9 @@ extern "C" pa_status pa_decode_no_alloc(void* out, const void* query, const void
   if (need > (size_t)PA_NO_ALLOC_WORKSPACE_BYTES) return PA_ERR_INVALID_ARG;
   void* ws = nullptr;
   if (need > 0 && (st = workspace_address(&ws)) != PA_OK) return st;
-  // Nothing in the array has to start at zero: the decode writes every
-  // partial it later reads.
+  // The array's first 256 bytes (the tensor-core kernel's work counter) must
+  // be zero before a call: static storage starts at zero and every call
+  // leaves them zero.  The partials after them need no initialisation.
   return pa_decode(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                    num_heads, scale, max_seq_len, partition_size, ws,
                    need > 0 ? (size_t)PA_NO_ALLOC_WORKSPACE_BYTES : 0, stream);

@@ -1,5 +1,5 @@
 // Tensor-core (tcgen05) decode kernels: bf16, head sizes 64 and 128, query
-// groups up to 16.
+// groups up to 16; a persistent grid sized by occupancy.
 #include <atomic>
 
 #include "decode_tc_kernel.cuh"
@@ -7,31 +7,59 @@
 
 namespace pa {
 
-template <int D>
-static cudaError_t launch_tc(dim3 grid, int smem_bytes, cudaStream_t stream,
-                             const CUtensorMap& map, const DecodeParams& params) {
+template <int D, int GP>
+static cudaError_t launch_tc(int num_sms, int smem_bytes, cudaStream_t stream,
+                             const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                             const DecodeParams& params) {
   static std::atomic<int> configured[64];
+  static std::atomic<int> per_sm[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem_bytes > configured[dev].load(std::memory_order_relaxed)) {
-    e = cudaFuncSetAttribute(paged_decode_tc_kernel<D>,
+    e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GP>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured[dev].store(smem_bytes, std::memory_order_relaxed);
+    int blocks = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_tc_kernel<D, GP>,
+                                                      kTcThreads, smem_bytes);
+    if (e != cudaSuccess) return e;
+    per_sm[dev].store(blocks < 1 ? 1 : blocks, std::memory_order_relaxed);
   }
-  paged_decode_tc_kernel<D><<<grid, kTcThreads, smem_bytes, stream>>>(map, params);
+  // Persistent grid: as many CTAs as fit at once, at most one per work item.
+  long long grid = (long long)num_sms * per_sm[dev].load(std::memory_order_relaxed);
+  if (grid > params.total_items) grid = params.total_items;
+  if (grid < 1) return cudaSuccess;
+  paged_decode_tc_kernel<D, GP><<<(unsigned)grid, kTcThreads, smem_bytes, stream>>>(kv_map, q_map,
+                                                                                   params);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_tc(int head_size, dim3 grid, int smem_bytes, cudaStream_t stream,
-                             const CUtensorMap& map, const DecodeParams& params,
-                             bool* supported) {
+template <int D>
+static cudaError_t launch_tc_group(int num_sms, int smem_bytes, cudaStream_t stream,
+                                   const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                                   const DecodeParams& params) {
+  const int g = params.group;
+  if (g <= 1) return launch_tc<D, 1>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+  if (g <= 2) return launch_tc<D, 2>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+  if (g <= 4) return launch_tc<D, 4>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+  if (g <= 8) return launch_tc<D, 8>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+  return launch_tc<D, 16>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+}
+
+cudaError_t launch_decode_tc(int head_size, int num_sms, int smem_bytes, cudaStream_t stream,
+                             const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                             const DecodeParams& params, bool* supported) {
   *supported = true;
   switch (head_size) {
-    case 64: return launch_tc<64>(grid, smem_bytes, stream, map, params);
-    case 128: return launch_tc<128>(grid, smem_bytes, stream, map, params);
+    case 64: return launch_tc_group<64>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+    case 128: return launch_tc_group<128>(num_sms, smem_bytes, stream, kv_map, q_map, params);
     default: *supported = false; return cudaSuccess;
   }
 }

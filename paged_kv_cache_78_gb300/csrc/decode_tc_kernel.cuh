@@ -1,4 +1,5 @@
-// Paged decode attention on the 5th-generation tensor cores (tcgen05, bf16).
+// Paged decode attention on the 5th-generation tensor cores (tcgen05, bf16),
+// persistent.
 //
 // The same operation as paged_decode_kernel (studying-code.tistory.com/16,
 // section "PagedAttention: 운영체제의 페이징 개념에서 영감을 받은 새로운 어텐션
@@ -9,22 +10,29 @@
 //   S^T [128 tokens x 16]   = K_tile [128 x D] . Q^T [D x 16]        (QK)
 //   O^T [D x 16]            = V_tile^T [D x 128] . P^T [128 x 16]     (PV)
 //
-// The 16 columns are the query heads of one KV head (G <= 16, padded with
-// zero rows).  One CTA = one (partition, KV head, sequence); six warps:
-//   warp 0      TMA producer: 128-token stages, one box per (block, 128-byte
-//               column group, K or V), written in the 128-byte swizzle that
-//               the MMA descriptors read directly (K tile: K-major A operand;
-//               V tile: M-major A operand);
-//   warp 1      tensor-memory allocator and MMA issuer (one thread): QK of
-//               stage k+1 is issued before PV of stage k, so the QK overlaps
-//               the softmax of stage k;
+// The 16 columns are the query heads of one KV head (G <= 16; rows past G
+// are masked).  A work item is one (partition, KV head, sequence).  The grid
+// is persistent: each CTA takes items from an atomic counter until they run
+// out, and its six warps stream every item's stages through one pipeline:
+//   warp 0      producer: takes the next item, publishes it in a 4-entry ring,
+//               loads the item's 16 query rows by TMA straight into the
+//               swizzled B-operand layout, and streams the item's 128-token
+//               K/V stages (one TMA box per block, 128-byte column group and
+//               K or V, in the 128-byte swizzle the MMA descriptors read),
+//               the boxes of a stage issued by all 32 lanes at once;
+//   warp 1      tensor-memory allocator and MMA issuer (one thread), an event
+//               loop that issues QK (up to two stages ahead) and PV (in order)
+//               as soon as each one's inputs are ready;
 //   warps 2..5  softmax warpgroup, one token (QK) or one head dimension (PV)
 //               per tensor-memory lane: online softmax in fp32 (log2 domain),
-//               P^T written to shared memory as bf16, and the PV result of each
-//               stage added into fp32 registers with the running rescale.
-// Tensor memory: S double buffer (2 x 16 columns), O double buffer (2 x 16).
-// Every wait is bounded; a timeout records PA_DEVERR_TIMEOUT, the CTA drains
-// its MMAs and TMA loads, frees its tensor memory and returns.
+//               P^T to shared memory as bf16, each stage's PV tile added into
+//               fp32 registers with the running rescale, and the item's output
+//               (final rows, or a split-KV partial) written at its end.
+// Stage ring slots, S/P/O double buffers and their barriers are indexed by a
+// stage counter that runs across items, so the pipeline never drains between
+// items.  Every wait is bounded; a timeout records PA_DEVERR_TIMEOUT, the CTA
+// drains its MMAs and TMA loads, frees its tensor memory and returns.  The
+// last CTA to finish resets the work counter, so it is zero for the next call.
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -35,30 +43,44 @@ namespace pa {
 constexpr int kTcTokens = 128;   // tokens per stage = M of the QK MMA
 constexpr int kTcHeads = 16;     // N of both MMAs: query heads, G padded
 constexpr int kTcThreads = 192;  // producer, MMA, 4 softmax warps
-constexpr int kTcTmemCols = 64;
+constexpr int kTcTmemCols = 64;  // S x2, O x2, 16 columns each
+constexpr int kTcItemRing = 4;
 
-// Shared-memory layout of the tensor-core decode kernel (byte offsets from
-// a 1024-aligned base).
+// Kinds of ring entries.
+constexpr int kItemAttend = 0;  // attention over tokens [tok0, tok1)
+constexpr int kItemZero = 1;    // a sequence of length 0: zero output rows
+constexpr int kItemEnd = 2;     // no more work
+
+struct TcItem {
+  int s, h, part, tok0, tok1, nstages, final_out, kind;
+};
+
+// Shared-memory layout (byte offsets from a 1024-aligned base).
 struct TcSmem {
-  int region;  // K (or V) tile of one stage
+  int region;    // K (or V) tile of one stage
   int stage;
-  int q_off;
-  int p_off;
-  int red_off;
+  int q_off;     // two Q tiles
+  int p_off;     // two P^T tiles
+  int red_off;   // max / sum exchange of the softmax warpgroup
+  int item_off;  // item ring
   int bar_off;
   int misc_off;
-  int total;   // bytes to request (includes 1024 of alignment slack)
+  int total;     // bytes to request (includes 1024 of alignment slack)
 };
 
 __host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages) {
   TcSmem l;
-  l.region = (head_size / 64) * kTcTokens * 128;
+  const int groups = head_size / 64;
+  l.region = groups * kTcTokens * 128;
   l.stage = 2 * l.region;
   l.q_off = num_stages * l.stage;
-  l.p_off = l.q_off + (head_size / 64) * kTcHeads * 128;
+  l.p_off = l.q_off + 2 * groups * kTcHeads * 128;
   l.red_off = l.p_off + 2 * 2 * kTcHeads * 128;
-  l.bar_off = l.red_off + 3 * 4 * kTcHeads * 4;
-  l.misc_off = l.bar_off + 8 * (2 * num_stages + 11);
+  l.item_off = l.red_off + 3 * 4 * kTcHeads * 4;
+  l.bar_off = l.item_off + kTcItemRing * (int)sizeof(TcItem);
+  // full[NS], empty[NS], s/p/o full/free and q full/free [2 each], item
+  // full/free [ring], drain
+  l.misc_off = l.bar_off + 8 * (2 * num_stages + 14 + 2 * kTcItemRing + 1);
   l.total = l.misc_off + 64 + 1024;
   return l;
 }
@@ -85,57 +107,68 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
-// MMA issuer: QK of stage k (S^T = K_tile . Q^T) into tensor-memory buffer
-// k % 2, once the stage has landed and that buffer has been read.
-template <int kKSteps, int kGroupBytes, uint32_t kIdesc>
-__device__ __forceinline__ bool tc_issue_qk(int k, int NS, uint32_t full0, uint32_t s_full,
-                                            uint32_t s_free, uint32_t sbase, int stage_bytes,
-                                            uint32_t q_s, uint32_t t_s, unsigned int* err) {
-  const int slot = k % NS;
-  const int sb = k & 1;
-  if (!mbar_wait_bounded(full0 + 8u * slot, (k / NS) & 1, err)) return false;
-  if (k >= 2 && !mbar_wait_bounded(s_free + 8u * sb, ((k >> 1) - 1) & 1, err)) return false;
-  tc::fence_after_sync();
-  const uint32_t ka = sbase + (uint32_t)slot * (uint32_t)stage_bytes;
-#pragma unroll
-  for (int kk = 0; kk < kKSteps; ++kk) {
-    const uint32_t goff = (uint32_t)((kk >> 2) * kGroupBytes) + (uint32_t)((kk & 3) * 32);
-    const uint64_t a = tc::smem_desc_sw128(ka + goff, 16, 1024);
-    const uint64_t b =
-        tc::smem_desc_sw128(q_s + (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32), 16, 1024);
-    tc::mma_bf16(t_s + 16u * sb, a, b, kIdesc, kk > 0);
-  }
-  tc::mma_commit(s_full + 8u * sb);
-  return true;
+// 3-D tiled tensor load (the query map), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
 }
 
-// Softmax warpgroup: add the PV tile of stage j (tensor-memory buffer j % 2)
-// into the fp32 accumulator, rescaled by that stage's factor.
-__device__ __forceinline__ bool tc_epilogue(int j, uint32_t o_full, uint32_t o_free,
-                                            uint32_t t_o_lane, unsigned int* err,
-                                            float (&o_acc)[kTcHeads],
-                                            const float (&alpha)[kTcHeads]) {
-  const int sb = j & 1;
-  const bool w = mbar_wait_bounded(o_full + 8u * sb, (j >> 1) & 1, err);
+// Barrier addresses of the tensor-core decode (shared-memory byte addresses).
+struct TcBars {
+  uint32_t full0, empty0, s_full, s_free, p_full, o_full, o_free, q_full, q_free, it_full,
+      it_free, drain;
+  __device__ __forceinline__ TcBars(uint32_t base, int ns) {
+    full0 = base;
+    empty0 = base + 8u * ns;
+    s_full = base + 16u * ns;
+    s_free = s_full + 16;
+    p_full = s_full + 32;
+    o_full = s_full + 48;
+    o_free = s_full + 64;
+    q_full = s_full + 80;
+    q_free = s_full + 96;
+    it_full = s_full + 112;
+    it_free = it_full + 8u * kTcItemRing;
+    drain = it_free + 8u * kTcItemRing;
+  }
+};
+
+// Softmax warpgroup: add the PV tile of global stage gk (tensor-memory buffer
+// gk % 2) into the fp32 accumulator, rescaled by that stage's factor.
+template <int GP>
+__device__ __forceinline__ bool tc_epilogue(int gk, const TcBars& b, uint32_t t_o_lane,
+                                            unsigned int* err, float (&o_acc)[GP],
+                                            const float (&alpha)[GP]) {
+  const int sb = gk & 1;
+  const bool w = mbar_wait_bounded(b.o_full + 8u * sb, (gk >> 1) & 1, err);
   __syncwarp();
   tc::fence_after_sync();
-  float ot[kTcHeads];
-  tc::tmem_ld16(t_o_lane + 16u * sb, ot);
+  float ot[GP];
+  tc::tmem_ld<GP>(t_o_lane + 16u * sb, ot);
   tc::tmem_wait_ld();
   tc::fence_before_sync();
-  mbar_arrive(o_free + 8u * sb);
+  mbar_arrive(b.o_free + 8u * sb);
 #pragma unroll
-  for (int g = 0; g < kTcHeads; ++g) o_acc[g] = fmaf(o_acc[g], alpha[g], ot[g]);
+  for (int g = 0; g < GP; ++g) o_acc[g] = fmaf(o_acc[g], alpha[g], ot[g]);
   return w;
 }
 
-template <int D>
+// GP: the query group size G rounded up to a power of two (1..16); the
+// softmax warpgroup handles GP heads (the MMAs always compute 16 columns).
+template <int D, int GP>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
+                           const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
   static_assert(D == 64 || D == 128, "tensor-core decode handles head sizes 64 and 128");
+  static_assert(GP >= 1 && GP <= kTcHeads && (GP & (GP - 1)) == 0, "padded group");
   constexpr int kGroups = D / 64;                 // 128-byte column groups of a row
   constexpr int kGroupBytes = kTcTokens * 128;    // one column group of a 128-token tile
   constexpr int kRegion = kGroups * kGroupBytes;  // K (or V) tile of a stage
+  constexpr int kQTile = kGroups * kTcHeads * 128;
   constexpr int kKSteps = D / 16;                 // QK: K = head dimension
   constexpr int kPvSteps = kTcTokens / 16;        // PV: K = tokens
   constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, kTcHeads, 0);
@@ -144,37 +177,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // group (D = 64) both halves read the same group and rows 64..127 repeat.
   constexpr uint32_t kPvLbo = kGroups > 1 ? kGroupBytes : 0;
 
-  const int part = blockIdx.x;
-  const int h = blockIdx.y;
-  const int s = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int G = p.group;
-
-  const int L = p.seq_lens[s];
-  const int P = p.partition_tokens;
-  const bool split = P > 0;
-  const int nparts = L <= 0 ? 0 : (split ? (L + P - 1) / P : 1);
-  const size_t row0 = (size_t)s * p.num_heads + (size_t)h * G;
-
-  if (L <= 0) {
-    if (part == 0) {
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + row0 * D;
-      for (int i = tid; i < G * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
-    }
-    return;
-  }
-  if ((split && nparts > p.max_parts) ||
-      ((L + p.block_size - 1) >> p.log2_block_size) > p.max_blocks_per_seq) {
-    if (part == 0 && tid == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
-    return;
-  }
-  if (part >= nparts) return;
-
-  const int tok0 = split ? part * P : 0;
-  const int tok1 = split ? min(L, tok0 + P) : L;
-  const int n_stages = (tok1 - tok0 + kTcTokens - 1) / kTcTokens;
   const int NS = p.num_stages;
   const TcSmem lay = tc_smem_layout(D, NS);
 
@@ -185,56 +191,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t q_s = sbase + lay.q_off;
   const uint32_t p_s = sbase + lay.p_off;
   float* red = reinterpret_cast<float*>(base + lay.red_off);  // [3][4 warps][16 heads]
-  const uint32_t bars = sbase + lay.bar_off;
-  const uint32_t full0 = bars;
-  const uint32_t empty0 = bars + 8u * NS;
-  const uint32_t s_full = bars + 16u * NS;   // [2]
-  const uint32_t s_free = s_full + 16;       // [2]
-  const uint32_t p_full = s_full + 32;       // [2]
-  const uint32_t o_full = s_full + 48;       // [2]
-  const uint32_t o_free = s_full + 64;       // [2]
-  const uint32_t drain = s_full + 80;
+  volatile TcItem* ring = reinterpret_cast<volatile TcItem*>(base + lay.item_off);
+  const TcBars bars(sbase + lay.bar_off, NS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + lay.misc_off);
   volatile int* flags = reinterpret_cast<volatile int*>(base + lay.misc_off + 16);
+  // flags[0] abort, flags[1] K/V stages issued, flags[2] Q tiles issued
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(full0 + 8u * i, 1);
-      mbar_init(empty0 + 8u * i, 1);
+      mbar_init(bars.full0 + 8u * i, 1);
+      mbar_init(bars.empty0 + 8u * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full + 8u * i, 1);
-      mbar_init(s_free + 8u * i, 128);
-      mbar_init(p_full + 8u * i, 128);
-      mbar_init(o_full + 8u * i, 1);
-      mbar_init(o_free + 8u * i, 128);
+      mbar_init(bars.s_full + 8u * i, 1);
+      mbar_init(bars.s_free + 8u * i, 128);
+      mbar_init(bars.p_full + 8u * i, 128);
+      mbar_init(bars.o_full + 8u * i, 1);
+      mbar_init(bars.o_free + 8u * i, 128);
+      mbar_init(bars.q_full + 8u * i, 1);
+      mbar_init(bars.q_free + 8u * i, 1);
     }
-    mbar_init(drain, 1);
-    flags[0] = 0;  // abort
-    flags[1] = 0;  // stages issued
+    for (int i = 0; i < kTcItemRing; ++i) {
+      mbar_init(bars.it_full + 8u * i, 1);
+      mbar_init(bars.it_free + 8u * i, 2);  // the MMA thread and the softmax warpgroup
+    }
+    mbar_init(bars.drain, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
     tc::tmem_alloc(smem_u32(tmem_slot), kTcTmemCols);
     tc::tmem_relinquish();
   }
-  if (tid == 32) tma_prefetch_desc(&kv_map);
-  // Q^T as the QK's B operand: [column group][16 rows][128 bytes], 128-byte
-  // swizzle (16-byte chunk c of row r stored at chunk c ^ (r % 8)); rows at or
-  // beyond G are zero.
-  {
-    const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.query) + row0 * D;
-    for (int i = tid; i < kTcHeads * D; i += blockDim.x) {
-      const int r = i / D;
-      const int d = i - r * D;
-      const __nv_bfloat16 v = r < G ? qg[r * D + d] : __float2bfloat16_rn(0.f);
-      const int col = d & 63;
-      const uint32_t addr = q_s + (uint32_t)((d >> 6) * kTcHeads * 128 + (r >> 3) * 1024 +
-                                             (r & 7) * 128 + ((((col >> 3) ^ (r & 7))) << 4) +
-                                             (col & 7) * 2);
-      st_shared_u16(addr, __bfloat16_as_ushort(v));
-    }
+  if (tid == 32) {
+    tma_prefetch_desc(&kv_map);
+    tma_prefetch_desc(&q_map);
   }
+  // Both P^T tiles start at zero: the softmax writes only rows below GP.
+  for (int i = tid; i < 2 * 2 * kTcHeads * 128 / 16; i += kTcThreads)
+    st_shared_zero16(p_s + (uint32_t)i * 16u);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
@@ -243,95 +240,277 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tS0 = tmem, tO0 = tmem + 32;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- producer ----------------
     const int BS = p.block_size;
     const int l2bs = p.log2_block_size;
     const int R = p.box_rows;  // min(block_size, 128)
     const int log2R = p.log2_box_rows;
-    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-    const int lb_end = (tok1 + BS - 1) >> l2bs;
-    int win = tok0 >> l2bs;
-    int cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
-    int nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
     const uint32_t box_bytes = (uint32_t)R * 128u;
-    int issued = 0;
-    for (int k = 0; k < n_stages; ++k) {
-      const int slot = k % NS;
-      if (k >= NS) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(empty0 + 8u * slot, ((k / NS) - 1) & 1, p.err);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok || flags[0]) {
-          flags[0] = 1;
-          break;
+    const int sh = p.num_seqs * p.num_kv_heads;
+    const int P = p.partition_tokens;
+    int gk = 0, qi = 0, ii = 0;
+    unsigned int idx = lane == 0 ? atomicAdd(p.sched, 1u) : 0u;
+    while (true) {
+      if (flags[0]) break;
+      // Lane 0 classifies the item; the warp follows its decision.
+      TcItem it{0, 0, 0, 0, 0, 0, 0, kItemEnd};
+      bool skip = false;
+      if (lane == 0 && idx < (unsigned)p.total_items) {
+        it.part = (int)(idx / (unsigned)sh);
+        const int rem = (int)(idx % (unsigned)sh);
+        it.s = rem / p.num_kv_heads;
+        it.h = rem - it.s * p.num_kv_heads;
+        const int L = p.seq_lens[it.s];
+        const int nparts = L <= 0 ? 0 : (P > 0 ? (L + P - 1) / P : 1);
+        if (L <= 0) {
+          it.kind = kItemZero;
+          skip = it.part != 0;
+        } else if ((P > 0 && nparts > p.max_parts) ||
+                   ((L + BS - 1) >> l2bs) > p.max_blocks_per_seq) {
+          if (it.part == 0 && it.h == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
+          skip = true;
+        } else if (it.part >= nparts) {
+          skip = true;
+        } else {
+          it.kind = kItemAttend;
+          it.tok0 = P > 0 ? it.part * P : 0;
+          it.tok1 = P > 0 ? min(L, it.tok0 + P) : L;
+          it.nstages = (it.tok1 - it.tok0 + kTcTokens - 1) / kTcTokens;
+          it.final_out = nparts == 1;
         }
       }
-      const int st_tok = tok0 + k * kTcTokens;
-      const int st_n = min(kTcTokens, tok1 - st_tok);
-      const int nbox = (st_n + R - 1) >> log2R;
-      if (lane == 0)
-        mbar_arrive_expect_tx(full0 + 8u * slot, (uint32_t)(nbox * kGroups * 2) * box_bytes);
-      const uint32_t kdst = sbase + (uint32_t)slot * (uint32_t)lay.stage;
-      for (int i = 0; i < nbox; ++i) {
-        const int tk = st_tok + (i << log2R);
-        const int lb = tk >> l2bs;
-        const int t0 = tk & (BS - 1);
-        while (lb >= win + 32) {
+      skip = __shfl_sync(0xffffffffu, skip, 0);
+      if (skip) {
+        if (lane == 0) idx = atomicAdd(p.sched, 1u);
+        continue;
+      }
+      it.s = __shfl_sync(0xffffffffu, it.s, 0);
+      it.h = __shfl_sync(0xffffffffu, it.h, 0);
+      it.part = __shfl_sync(0xffffffffu, it.part, 0);
+      it.tok0 = __shfl_sync(0xffffffffu, it.tok0, 0);
+      it.tok1 = __shfl_sync(0xffffffffu, it.tok1, 0);
+      it.nstages = __shfl_sync(0xffffffffu, it.nstages, 0);
+      it.final_out = __shfl_sync(0xffffffffu, it.final_out, 0);
+      it.kind = __shfl_sync(0xffffffffu, it.kind, 0);
+      // Publish it in the ring.
+      const int j = ii % kTcItemRing;
+      bool ok = true;
+      if (lane == 0) {
+        if (ii >= kTcItemRing)
+          ok = mbar_wait_bounded(bars.it_free + 8u * j, ((ii / kTcItemRing) - 1) & 1, p.err);
+        if (ok) {
+          ring[j].s = it.s;
+          ring[j].h = it.h;
+          ring[j].part = it.part;
+          ring[j].tok0 = it.tok0;
+          ring[j].tok1 = it.tok1;
+          ring[j].nstages = it.nstages;
+          ring[j].final_out = it.final_out;
+          ring[j].kind = it.kind;
+          mbar_arrive(bars.it_full + 8u * j);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        flags[0] = 1;
+        break;
+      }
+      ++ii;
+      if (it.kind == kItemEnd) break;
+      if (lane == 0) idx = atomicAdd(p.sched, 1u);  // next item, fetched early
+      if (it.kind != kItemAttend) continue;
+
+      // Query rows h*G .. h*G+15 of sequence s (rows past G are masked).
+      const int qb = qi & 1;
+      if (lane == 0) {
+        if (qi >= 2) ok = mbar_wait_bounded(bars.q_free + 8u * qb, ((qi >> 1) - 1) & 1, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(bars.q_full + 8u * qb, (uint32_t)kQTile);
+          const int row0 = it.s * p.num_heads + it.h * G;
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g)
+            tma_load_3d(q_s + (uint32_t)(qb * kQTile + g * kTcHeads * 128), &q_map,
+                        bars.q_full + 8u * qb, 0, g, row0);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        flags[0] = 1;
+        break;
+      }
+      ++qi;
+      if (lane == 0) flags[2] = qi;
+
+      // The item's K/V stages.  Every lane issues TMA boxes (a box = one
+      // block's rows of one 128-byte column group of K or of V): one thread
+      // issuing them in sequence cannot keep HBM busy.  The block table is
+      // cached in two 32-entry register windows, [win, win+32) in `cur` and
+      // [win+32, win+64) in `nxt`; a stage spans at most 16 blocks.
+      const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+      const int lb_end = (it.tok1 + BS - 1) >> l2bs;
+      int win = it.tok0 >> l2bs;
+      int cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
+      int nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+      constexpr int kOpsPerBox = kGroups * 2;
+      for (int k = 0; k < it.nstages; ++k, ++gk) {
+        const int slot = gk % NS;
+        if (gk >= NS) {
+          if (lane == 0) ok = mbar_wait_bounded(bars.empty0 + 8u * slot, ((gk / NS) - 1) & 1, p.err);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+        const int st_tok = it.tok0 + k * kTcTokens;
+        const int st_n = min(kTcTokens, it.tok1 - st_tok);
+        const int nbox = (st_n + R - 1) >> log2R;
+        const int lb0 = st_tok >> l2bs;
+        while (lb0 >= win + 32) {
           cur = nxt;
           win += 32;
           nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
         }
-        const int id = __shfl_sync(0xffffffffu, cur, lb - win);
-        if (lane == 0) {
-          int ck = id, cv = p.num_blocks + id;
-          if (id < 0 || id >= p.num_blocks) {
-            record_error(p.err, PA_DEVERR_BLOCK_ID);
-            ck = cv = 2 * p.num_blocks;  // outside the tensor: zero fill
-          }
-#pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-            const uint32_t dst = kdst + (uint32_t)(g * kGroupBytes) + (uint32_t)i * box_bytes;
-            tma_load_5d(dst, &kv_map, full0 + 8u * slot, 0, g, h, t0, ck);
-            tma_load_5d(dst + kRegion, &kv_map, full0 + 8u * slot, 0, g, h, t0, cv);
+        if (lane == 0)
+          mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)(nbox * kOpsPerBox) * box_bytes);
+        __syncwarp();
+        const uint32_t kdst = sbase + (uint32_t)slot * (uint32_t)lay.stage;
+        const int nops = nbox * kOpsPerBox;
+        for (int b0 = 0; b0 < nops; b0 += 32) {
+          const int op = b0 + lane;
+          const bool live = op < nops;
+          const int i = live ? op / kOpsPerBox : 0;
+          const int r = op - i * kOpsPerBox;
+          const int tk = st_tok + (i << log2R);
+          const int src = (tk >> l2bs) - win;  // 0 .. 47
+          const int id_cur = __shfl_sync(0xffffffffu, cur, src & 31);
+          const int id_nxt = __shfl_sync(0xffffffffu, nxt, src & 31);
+          if (live) {
+            const int id = src < 32 ? id_cur : id_nxt;
+            const int g = r >> 1;
+            const int kv = r & 1;
+            int c4 = kv * p.num_blocks + id;
+            if (id < 0 || id >= p.num_blocks) {
+              record_error(p.err, PA_DEVERR_BLOCK_ID);
+              c4 = 2 * p.num_blocks;  // outside the tensor: zero fill
+            }
+            const uint32_t dst = kdst + (uint32_t)(kv * kRegion + g * kGroupBytes) +
+                                 (uint32_t)i * box_bytes;
+            tma_load_5d(dst, &kv_map, bars.full0 + 8u * slot, 0, g, it.h, tk & (BS - 1), c4);
           }
         }
+        if (lane == 0) flags[1] = gk + 1;
       }
-      issued = k + 1;
+      if (!ok) {
+        flags[0] = 1;
+        break;
+      }
     }
-    if (lane == 0) flags[1] = issued;
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // An event loop: QK of the next stage and PV of the oldest stage are
+    // issued as soon as their inputs are ready, independently, so a PV never
+    // waits for an unrelated TMA load (PV releases the stage slot the loads
+    // refill).  QK runs at most two stages ahead (S is double-buffered).
     if (lane == 0) {
-      bool ok = true;
-      if (n_stages > 0) ok = tc_issue_qk<kKSteps, kGroupBytes, kIdescQK>(0, NS, full0, s_full, s_free, sbase, lay.stage, q_s, tS0, p.err);
-      for (int k = 0; ok && k < n_stages; ++k) {
-        if (k + 1 < n_stages &&
-            !(ok = tc_issue_qk<kKSteps, kGroupBytes, kIdescQK>(k + 1, NS, full0, s_full, s_free,
-                                                              sbase, lay.stage, q_s, tS0, p.err)))
-          break;
-        const int slot = k % NS;
-        const int sb = k & 1;
-        if (!(ok = mbar_wait_bounded(p_full + 8u * sb, (k >> 1) & 1, p.err))) break;
-        if (k >= 2 && !(ok = mbar_wait_bounded(o_free + 8u * sb, ((k >> 1) - 1) & 1, p.err)))
-          break;
-        tc::fence_after_sync();
-        const uint32_t va = sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)kRegion;
-        const uint32_t pa_ = p_s + (uint32_t)sb * 2u * kTcHeads * 128u;
-#pragma unroll
-        for (int kk = 0; kk < kPvSteps; ++kk) {
-          const uint64_t a = tc::smem_desc_sw128(va + (uint32_t)kk * 2048u, kPvLbo, 1024);
-          const uint64_t b = tc::smem_desc_sw128(
-              pa_ + (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32), 16, 1024);
-          tc::mma_bf16(tO0 + 16u * sb, a, b, kIdescPV, kk > 0);
+      int next_qk = 0, next_pv = 0;  // global stage counters
+      int ii = 0, qi = 0, qb = 0, qk_k = 0, qk_n = 0;
+      bool have_item = false, need_q = false, end_seen = false, ok = true;
+      long long t_idle = clock64();
+      while (true) {
+        bool progress = false;
+        if (!have_item && !end_seen) {
+          const int j = ii % kTcItemRing;
+          if (mbar_test(bars.it_full + 8u * j, (ii / kTcItemRing) & 1)) {
+            const int kind = ring[j].kind;
+            const int n = ring[j].nstages;
+            mbar_arrive(bars.it_free + 8u * j);
+            ++ii;
+            progress = true;
+            if (kind == kItemEnd) {
+              end_seen = true;
+            } else if (kind == kItemAttend) {
+              have_item = true;
+              need_q = true;
+              qk_k = 0;
+              qk_n = n;
+              qb = qi & 1;
+            }
+          }
         }
-        tc::mma_commit(o_full + 8u * sb);
-        tc::mma_commit(empty0 + 8u * slot);
+        if (have_item && need_q && mbar_test(bars.q_full + 8u * qb, (qi >> 1) & 1)) {
+          need_q = false;
+          progress = true;
+        }
+        if (have_item && !need_q && next_qk < next_pv + 2) {
+          const int gk = next_qk;
+          const int slot = gk % NS;
+          const int sb = gk & 1;
+          if (mbar_test(bars.full0 + 8u * slot, (gk / NS) & 1) &&
+              (gk < 2 || mbar_test(bars.s_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+            tc::fence_after_sync();
+            const uint32_t ka = sbase + (uint32_t)slot * (uint32_t)lay.stage;
+            const uint32_t q_tile = q_s + (uint32_t)(qb * kQTile);
+#pragma unroll
+            for (int kk = 0; kk < kKSteps; ++kk) {
+              const uint32_t goff = (uint32_t)((kk >> 2) * kGroupBytes) + (uint32_t)((kk & 3) * 32);
+              const uint64_t a = tc::smem_desc_sw128(ka + goff, 16, 1024);
+              const uint64_t bd = tc::smem_desc_sw128(
+                  q_tile + (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32), 16, 1024);
+              tc::mma_bf16(tS0 + 16u * sb, a, bd, kIdescQK, kk > 0);
+            }
+            tc::mma_commit(bars.s_full + 8u * sb);
+            ++next_qk;
+            if (++qk_k == qk_n) {
+              tc::mma_commit(bars.q_free + 8u * qb);  // the item's Q tile is no longer read
+              ++qi;
+              have_item = false;
+            }
+            progress = true;
+          }
+        }
+        if (next_pv < next_qk) {
+          const int gk = next_pv;
+          const int slot = gk % NS;
+          const int sb = gk & 1;
+          if (mbar_test(bars.p_full + 8u * sb, (gk >> 1) & 1) &&
+              (gk < 2 || mbar_test(bars.o_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+            tc::fence_after_sync();
+            const uint32_t va = sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)kRegion;
+            const uint32_t pt = p_s + (uint32_t)sb * 2u * kTcHeads * 128u;
+#pragma unroll
+            for (int kk = 0; kk < kPvSteps; ++kk) {
+              const uint64_t a = tc::smem_desc_sw128(va + (uint32_t)kk * 2048u, kPvLbo, 1024);
+              const uint64_t bd = tc::smem_desc_sw128(
+                  pt + (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32), 16, 1024);
+              tc::mma_bf16(tO0 + 16u * sb, a, bd, kIdescPV, kk > 0);
+            }
+            tc::mma_commit(bars.o_full + 8u * sb);
+            tc::mma_commit(bars.empty0 + 8u * slot);
+            ++next_pv;
+            progress = true;
+          }
+        }
+        if (end_seen && !have_item && next_pv == next_qk) break;
+        if (progress) {
+          t_idle = clock64();
+        } else if (!flags[0]) {
+          // Nothing ready: back off instead of spinning, leaving issue slots
+          // to the softmax warp that shares this warp's scheduler.
+          __nanosleep(64);
+        }
+        if (progress) {
+        } else if (flags[0]) {
+          ok = false;
+          break;
+        } else if (clock64() - t_idle > kWaitLimitCycles) {
+          record_error(p.err, PA_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
       }
       if (!ok) flags[0] = 1;
       // Every MMA this thread issued completes before the CTA may free its
       // tensor memory.
-      tc::mma_commit(drain);
-      mbar_wait_bounded(drain, 0, p.err);
+      tc::mma_commit(bars.drain);
+      mbar_wait_bounded(bars.drain, 0, p.err);
     }
     __syncwarp();
   } else {
@@ -339,137 +518,167 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q4 = warp & 3;                  // tensor-memory lane quarter
     const int row = q4 * 32 + lane;           // token (QK) / head dimension (PV)
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-    float m_run[kTcHeads], l_run[kTcHeads], o_acc[kTcHeads], alpha_prev[kTcHeads];
-#pragma unroll
-    for (int g = 0; g < kTcHeads; ++g) {
-      m_run[g] = -INFINITY;
-      l_run[g] = 0.f;
-      o_acc[g] = 0.f;
-      alpha_prev[g] = 1.f;
-    }
+    const uint32_t tO_lane = tO0 + lane_addr;
+    float* red2 = red + 2 * 4 * kTcHeads;
+    int gk = 0;
     bool ok = true;
-
-    for (int k = 0; k < n_stages; ++k) {
-      const int sb = k & 1;
-      const int slot = k % NS;
-      bool w = mbar_wait_bounded(s_full + 8u * sb, (k >> 1) & 1, p.err);
-      __syncwarp();
-      tc::fence_after_sync();
-      float sc[kTcHeads];
-      tc::tmem_ld16(tS0 + 16u * sb + lane_addr, sc);
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      mbar_arrive(s_free + 8u * sb);
-
-      const int nvalid = min(kTcTokens, tok1 - (tok0 + k * kTcTokens));
-      const bool valid = row < nvalid;
-      if (!valid) {
-        // A stale row of V (past the sequence, or never loaded) must not reach
-        // the PV product: 0 * NaN would.
-        const uint32_t vrow = sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)kRegion +
-                              (uint32_t)row * 128u;
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_zero16(vrow + (uint32_t)(g * kGroupBytes + c * 16));
+    for (int ii = 0;; ++ii) {
+      const int j = ii % kTcItemRing;
+      const bool w = mbar_wait_bounded(bars.it_full + 8u * j, (ii / kTcItemRing) & 1, p.err);
+      TcItem it;
+      it.s = ring[j].s;
+      it.h = ring[j].h;
+      it.part = ring[j].part;
+      it.tok0 = ring[j].tok0;
+      it.tok1 = ring[j].tok1;
+      it.nstages = ring[j].nstages;
+      it.final_out = ring[j].final_out;
+      it.kind = ring[j].kind;
+      ok = softmax_group_all(w && ok && !flags[0]);  // every thread has read the entry
+      if (!ok) break;
+      if (tid == 64) mbar_arrive(bars.it_free + 8u * j);
+      if (it.kind == kItemEnd) break;
+      const size_t row0 = (size_t)it.s * p.num_heads + (size_t)it.h * G;
+      if (it.kind == kItemZero) {
+        if (row < D)
+          for (int g = 0; g < G; ++g)
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(row0 + g) * D + row] = __float2bfloat16_rn(0.f);
+        continue;
       }
-      float x[kTcHeads];
+
+      float m_run[GP], l_run[GP], o_acc[GP], alpha_prev[GP];
 #pragma unroll
-      for (int g = 0; g < kTcHeads; ++g)
-        x[g] = (valid && g < G) ? sc[g] * p.scale_log2 : -INFINITY;
-      float* redk = red + sb * 4 * kTcHeads;
+      for (int g = 0; g < GP; ++g) {
+        m_run[g] = -INFINITY;
+        l_run[g] = 0.f;
+        o_acc[g] = 0.f;
+        alpha_prev[g] = 1.f;
+      }
+      const int n = it.nstages;
+      for (int k = 0; k < n; ++k) {
+        const int g_k = gk + k;
+        const int sb = g_k & 1;
+        const int slot = g_k % NS;
+        const bool ws = mbar_wait_bounded(bars.s_full + 8u * sb, (g_k >> 1) & 1, p.err);
+        __syncwarp();
+        tc::fence_after_sync();
+        float sc[GP];
+        tc::tmem_ld<GP>(tS0 + 16u * sb + lane_addr, sc);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        mbar_arrive(bars.s_free + 8u * sb);
+
+        const int nvalid = min(kTcTokens, it.tok1 - (it.tok0 + k * kTcTokens));
+        const bool valid = row < nvalid;
+        if (!valid) {
+          // A stale row of V (past the sequence, or never loaded) must not
+          // reach the PV product: 0 * NaN would.
+          const uint32_t vrow = sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)kRegion +
+                                (uint32_t)row * 128u;
 #pragma unroll
-      for (int g = 0; g < kTcHeads; ++g) {
-        if (g < G) {
+          for (int g = 0; g < kGroups; ++g)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_shared_zero16(vrow + (uint32_t)(g * kGroupBytes + c * 16));
+        }
+        float x[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+          x[g] = (valid && g < G) ? sc[g] * p.scale_log2 : -INFINITY;
+        float* redk = red + sb * 4 * kTcHeads;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
           const float wm = warp_max(x[g]);
           if (lane == 0) redk[q4 * kTcHeads + g] = wm;
         }
-      }
-      if (!softmax_group_all(w && ok && !flags[0])) {
-        ok = false;
-        break;
-      }
-      float alpha[kTcHeads], pr[kTcHeads];
+        if (!(ok = softmax_group_all(ws && ok && !flags[0]))) break;
+        float alpha[GP], pr[GP];
 #pragma unroll
-      for (int g = 0; g < kTcHeads; ++g) {
-        if (g < G) {
+        for (int g = 0; g < GP; ++g) {
+          // Heads g >= G are padding: their scores are all -inf, the
+          // maximum stays -inf, and they are given weight 0 and factor 1.
           const float tmax = fmaxf(fmaxf(redk[g], redk[kTcHeads + g]),
                                    fmaxf(redk[2 * kTcHeads + g], redk[3 * kTcHeads + g]));
           const float m_new = fmaxf(m_run[g], tmax);
-          alpha[g] = fast_exp2(m_run[g] - m_new);
+          const bool real = g < G;
+          alpha[g] = real ? fast_exp2(m_run[g] - m_new) : 1.f;
           m_run[g] = m_new;
           // The weight enters P.V rounded to bf16; the denominator sums the
           // same rounded weights, so the output stays a convex combination.
-          pr[g] = __bfloat162float(__float2bfloat16_rn(fast_exp2(x[g] - m_new)));
+          pr[g] = real ? __bfloat162float(__float2bfloat16_rn(fast_exp2(x[g] - m_new))) : 0.f;
           l_run[g] = fmaf(l_run[g], alpha[g], pr[g]);
-        } else {
-          alpha[g] = 1.f;
-          pr[g] = 0.f;
         }
-      }
-      // P^T as the PV's B operand: [64-token group][16 rows][128 bytes], swizzled.
-      {
-        const uint32_t pb = p_s + (uint32_t)sb * 2u * kTcHeads * 128u +
-                            (uint32_t)((row >> 6) * kTcHeads * 128);
-        const int col = row & 63;
+        // P^T as the PV's B operand: [64-token group][16 rows][128 bytes], swizzled.
+        {
+          const uint32_t pb = p_s + (uint32_t)sb * 2u * kTcHeads * 128u +
+                              (uint32_t)((row >> 6) * kTcHeads * 128);
+          const int col = row & 63;
 #pragma unroll
-        for (int g = 0; g < kTcHeads; ++g) {
-          const uint32_t addr = pb + (uint32_t)((g >> 3) * 1024 + (g & 7) * 128 +
-                                                ((((col >> 3) ^ (g & 7))) << 4) + (col & 7) * 2);
-          st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr[g])));
+          for (int g = 0; g < GP; ++g) {
+            const uint32_t addr = pb + (uint32_t)((g >> 3) * 1024 + (g & 7) * 128 +
+                                                  ((((col >> 3) ^ (g & 7))) << 4) + (col & 7) * 2);
+            st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr[g])));
+          }
         }
-      }
-      tc::fence_proxy_async_smem();
-      mbar_arrive(p_full + 8u * sb);
-      if (k >= 1) ok = tc_epilogue(k - 1, o_full, o_free, tO0 + lane_addr, p.err, o_acc, alpha_prev) && ok;
+        tc::fence_proxy_async_smem();
+        mbar_arrive(bars.p_full + 8u * sb);
+        if (k >= 1) ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, o_acc, alpha_prev) && ok;
 #pragma unroll
-      for (int g = 0; g < kTcHeads; ++g) alpha_prev[g] = alpha[g];
-    }
-    // The last PV tile; the decision is taken by the whole warpgroup so that
-    // every warp executes the tensor-memory load convergently or not at all.
-    ok = softmax_group_all(ok && !flags[0]);
-    if (ok && n_stages > 0)
-      ok = tc_epilogue(n_stages - 1, o_full, o_free, tO0 + lane_addr, p.err, o_acc, alpha_prev);
+        for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
+      }
+      if (!ok) break;
+      // The item's last PV tile; decided by the whole warpgroup so that every
+      // warp executes the tensor-memory load convergently or not at all.
+      if (!(ok = softmax_group_all(ok && !flags[0]))) break;
+      ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, o_acc, alpha_prev);
+      gk += n;
 
-    // l over the warpgroup's 128 token rows.
-    float* red2 = red + 2 * 4 * kTcHeads;
+      // l over the warpgroup's 128 token rows, then the item's output.
 #pragma unroll
-    for (int g = 0; g < kTcHeads; ++g) {
-      if (g < G) {
-        const float ws = warp_sum(l_run[g]);
-        if (lane == 0) red2[q4 * kTcHeads + g] = ws;
+      for (int g = 0; g < GP; ++g) {
+        const float s_ = warp_sum(l_run[g]);
+        if (lane == 0) red2[q4 * kTcHeads + g] = s_;
       }
-    }
-    ok = softmax_group_all(ok && !flags[0]);
-    if (!ok) {
-      flags[0] = 1;
-    } else if (row < D) {
-      const int d = row;
+      if (!(ok = softmax_group_all(ok && !flags[0]))) break;
+      if (row < D) {
+        const int d = row;
 #pragma unroll
-      for (int g = 0; g < kTcHeads; ++g) {
-        if (g >= G) continue;
-        const float lsum = red2[g] + red2[kTcHeads + g] + red2[2 * kTcHeads + g] +
-                           red2[3 * kTcHeads + g];
-        const float val = o_acc[g] / lsum;
-        if (nparts == 1) {
-          reinterpret_cast<__nv_bfloat16*>(p.out)[(row0 + g) * D + d] = __float2bfloat16_rn(val);
-        } else {
-          const size_t prow = (row0 + g) * (size_t)p.max_parts + part;
-          p.part_o[prow * D + d] = val;
-          if (d == 0) p.part_lse[prow] = m_run[g] + log2f(lsum);
+        for (int g = 0; g < GP; ++g) {
+          if (g >= G) continue;
+          const float lsum = red2[g] + red2[kTcHeads + g] + red2[2 * kTcHeads + g] +
+                             red2[3 * kTcHeads + g];
+          const float val = o_acc[g] / lsum;
+          if (it.final_out) {
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(row0 + g) * D + d] = __float2bfloat16_rn(val);
+          } else {
+            const size_t prow = (row0 + g) * (size_t)p.max_parts + it.part;
+            p.part_o[prow * D + d] = val;
+            if (d == 0) p.part_lse[prow] = m_run[g] + log2f(lsum);
+          }
         }
       }
     }
+    if (!ok) flags[0] = 1;
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (flags[0] && tid == 0) {
-    // Wait (bounded) for every TMA load this CTA issued.
-    const int issued = flags[1];
-    for (int sl = 0; sl < NS && sl < issued; ++sl) {
-      const int last_use = (issued - 1 - sl) / NS;
-      mbar_wait_bounded(full0 + 8u * sl, last_use & 1, p.err);
+  if (tid == 0) {
+    if (flags[0]) {
+      // Wait (bounded) for every TMA load this CTA issued.
+      const int issued = flags[1];
+      for (int sl = 0; sl < NS && sl < issued; ++sl)
+        mbar_wait_bounded(bars.full0 + 8u * sl, ((issued - 1 - sl) / NS) & 1, p.err);
+      const int qissued = flags[2];
+      for (int b = 0; b < 2 && b < qissued; ++b)
+        mbar_wait_bounded(bars.q_full + 8u * b, ((qissued - 1 - b) / 2) & 1, p.err);
+    }
+    // The last CTA to finish resets the work counter for the next call.
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      p.sched[0] = 0u;
+      p.sched[1] = 0u;
+      __threadfence();
     }
   }
   if (warp == 1) {

@@ -29,9 +29,9 @@ cudaError_t launch_decode_f32(int head_size, int group, dim3 grid, int smem_byte
                               const DecodeParams& params, bool* supported);
 
 // Tensor-core decode (bf16, head size 64 or 128, group <= 16).
-cudaError_t launch_decode_tc(int head_size, dim3 grid, int smem_bytes, cudaStream_t stream,
-                             const CUtensorMap& map, const DecodeParams& params,
-                             bool* supported);
+cudaError_t launch_decode_tc(int head_size, int num_sms, int smem_bytes, cudaStream_t stream,
+                             const CUtensorMap& kv_map, const CUtensorMap& q_map,
+                             const DecodeParams& params, bool* supported);
 
 cudaError_t launch_lse_reduce(int dtype, int head_size, void* out, const float* part_o,
                               const float* part_lse, const int32_t* seq_lens, int num_seqs,

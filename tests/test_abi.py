@@ -79,8 +79,8 @@ def test_partition_and_workspace_sizes():
         pa.pa_decode_partition_size(d, 8, 32, 32768, 520)           # not a multiple of 16
     nbytes = pa.pa_decode_workspace_size(d, 8, 32, 32768, 512)
     rows = 8 * 32 * 64
-    assert nbytes == -(-rows * 128 * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
-    assert pa.pa_decode_workspace_size(d, 8, 32, 300, 512) == 0
+    assert nbytes == 256 + -(-rows * 128 * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+    assert pa.pa_decode_workspace_size(d, 8, 32, 300, 512) == 256   # header only
 
 
 def test_zero_work_calls_are_noops():
