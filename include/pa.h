@@ -155,7 +155,7 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
 
 /* Kernel families for pa_decode_ex. */
 typedef enum pa_decode_kernel {
-  PA_KERNEL_AUTO = 0,   /* CUDA cores for groups up to 8, tensor cores for groups of 9..16 */
+  PA_KERNEL_AUTO = 0,   /* tensor cores where supported and G >= 2, else CUDA cores */
   PA_KERNEL_SIMT = 1,   /* CUDA cores: fp32 dot products and accumulation; group <= 8 */
   PA_KERNEL_TENSOR = 2  /* 5th-generation tensor cores: bf16 only, head size 64 or 128,
                            group <= 16, block_size >= 8; scores and P.V accumulate in fp32,
@@ -291,6 +291,21 @@ int32_t pa_pool_num_free(const pa_pool* pool);
  * ------------------------------------------------------------------------- */
 pa_status pa_get_device_error(uint32_t* flags, void* stream);
 const char* pa_status_string(pa_status status);
+
+/* Timeline of the tensor-core decode, for performance work.  After a call
+ * with a non-NULL device buffer, every tensor-core pa_decode of this process
+ * records, per CTA and per role (0 producer, 1 MMA issuer, 2 softmax
+ * warpgroup), its first events_per_role events as two 64-bit words
+ *     buf[((cta * 3 + role) * events_per_role + i) * 2 + 0] = SM clock (clock64)
+ *     buf[((cta * 3 + role) * events_per_role + i) * 2 + 1] = tag << 32 | argument
+ * Tags (argument): 1 item published (item number), 2 stage loads issued
+ * (stage), 3 QK issued (stage), 4 PV issued (stage), 5 scores read (stage),
+ * 6 P written (stage), 7 item output written (item number), 8 producer done
+ * (items), 9 CTA start (low 32 bits of the global timer, ns).  Entries
+ * beyond a role's events are left as they were.  A launch whose grid needs
+ * more than `bytes` records nothing.  NULL turns tracing off (the default).
+ * Host-side setting shared by all threads of the process. */
+pa_status pa_set_decode_trace(void* device_buffer, size_t bytes, int32_t events_per_role);
 /* Library version, e.g. "0.1.0". */
 const char* pa_version(void);
 

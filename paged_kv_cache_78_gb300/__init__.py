@@ -45,7 +45,7 @@ EXPORTS = (
     "pa_pool_add_seq", "pa_pool_fork", "pa_pool_append_token", "pa_pool_append_tokens",
     "pa_pool_free_seq", "pa_pool_block_table", "pa_pool_fill_tables", "pa_pool_slot",
     "pa_pool_ref_count", "pa_pool_num_free", "pa_get_device_error", "pa_status_string",
-    "pa_version",
+    "pa_version", "pa_set_decode_trace",
 )
 
 
@@ -94,6 +94,7 @@ def _load() -> ctypes.CDLL:
         "pa_pool_slot": [vp, i64, i64, p_i64],
         "pa_pool_ref_count": [vp, i32, p_i32],
         "pa_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
+        "pa_set_decode_trace": [vp, sz, i32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -401,3 +402,14 @@ def tensor_core_supported(cache: torch.Tensor, num_heads: int) -> bool:
     d = cache_desc(cache)
     g = num_heads // d.num_kv_heads
     return d.dtype == PA_BF16 and d.head_size in (64, 128) and g <= 16 and d.block_size >= 8
+
+
+def pa_set_decode_trace(buffer: torch.Tensor | None, events_per_role: int = 0) -> None:
+    """Record the tensor-core decode's timeline into `buffer` (a CUDA tensor;
+    see include/pa.h for the record format), or stop recording (None)."""
+    if buffer is None:
+        _check(lib.pa_set_decode_trace(None, 0, 0), "pa_set_decode_trace")
+        return
+    _check(lib.pa_set_decode_trace(_dev_ptr(buffer, "buffer"),
+                                   buffer.numel() * buffer.element_size(), int(events_per_role)),
+           "pa_set_decode_trace")

@@ -35,6 +35,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// Timeline buffer of the tensor-core decode (pa_set_decode_trace).
+std::atomic<void*> g_trace_buf{nullptr};
+std::atomic<size_t> g_trace_bytes{0};
+std::atomic<int> g_trace_per_role{0};
+
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 int ilog2(int x) {
   int r = 0;
@@ -136,6 +141,15 @@ size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_p
 extern "C" {
 
 const char* pa_version(void) { return "0.1.0"; }
+
+pa_status pa_set_decode_trace(void* device_buffer, size_t bytes, int32_t events_per_role) {
+  if (device_buffer && (events_per_role < 1 || bytes < 16 || !aligned(device_buffer, 8)))
+    return PA_ERR_INVALID_ARG;
+  g_trace_per_role.store(device_buffer ? events_per_role : 0);
+  g_trace_bytes.store(device_buffer ? bytes : 0);
+  g_trace_buf.store(device_buffer);
+  return PA_OK;
+}
 
 const char* pa_status_string(pa_status s) {
   switch (s) {
@@ -277,10 +291,10 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   } else if (kernel == PA_KERNEL_SIMT) {
     use_tc = false;
   } else {
-    // Automatic choice: the tensor-core kernel where only it applies (groups
-    // of 9..16); elsewhere the CUDA-core kernel, which measures faster on the
-    // benchmark workloads in its present one-CTA-per-partition form.
-    use_tc = tc_ok && group > 8;
+    // Automatic choice: the tensor-core kernel for grouped queries (G >= 2),
+    // whose CUDA-core cost grows with G; the CUDA-core kernel for G = 1,
+    // where it measures faster.
+    use_tc = tc_ok && group >= 2;
   }
   if (!use_tc && group > 8) return PA_ERR_UNSUPPORTED;
 
@@ -318,6 +332,9 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
     prm.num_consumers = 1;
     smem = pa::tc_smem_layout(D, prm.num_stages).total;
     prm.sched = sched;
+    prm.trace = static_cast<unsigned long long*>(g_trace_buf.load());
+    prm.trace_per_role = g_trace_per_role.load();
+    prm.trace_bytes = g_trace_bytes.load();
     prm.total_items = (int)std::min<long long>((long long)num_seqs * desc->num_kv_heads * max_parts,
                                                (1ll << 31) - 1);
   } else {

@@ -52,6 +52,9 @@ struct DecodeParams {
   unsigned int* sched;          // tensor-core kernel: [0] next work item, [1] CTAs finished
   int total_items;              // tensor-core kernel: num_seqs * num_kv_heads * max_parts
   int num_seqs;
+  unsigned long long* trace;    // tensor-core kernel timeline, or null
+  int trace_per_role;
+  size_t trace_bytes;
   int num_blocks;
   int block_size;
   int log2_block_size;

@@ -1,5 +1,6 @@
 // Tensor-core (tcgen05) decode kernels: bf16, head sizes 64 and 128, query
 // groups up to 16; a persistent grid sized by occupancy.
+#include <algorithm>
 #include <atomic>
 
 #include "decode_tc_kernel.cuh"
@@ -26,18 +27,32 @@ static cudaError_t launch_tc(int num_sms, int smem_bytes, cudaStream_t stream,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     configured[dev].store(smem_bytes, std::memory_order_relaxed);
-    int blocks = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_tc_kernel<D, GP>,
-                                                      kTcThreads, smem_bytes);
+    // Resident CTAs per SM: bounded by shared memory (plus the 1 KB the
+    // driver reserves per CTA), registers and tensor-memory columns.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, paged_decode_tc_kernel<D, GP>);
     if (e != cudaSuccess) return e;
+    int smem_per_sm = 0, regs_per_sm = 0;
+    e = cudaDeviceGetAttribute(&smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+    int blocks = smem_per_sm / (smem_bytes + 1024);
+    blocks = std::min(blocks, regs_per_sm / (regs_per_warp * (kTcThreads / 32)));
+    blocks = std::min(blocks, 512 / kTcTmemCols);
     per_sm[dev].store(blocks < 1 ? 1 : blocks, std::memory_order_relaxed);
   }
   // Persistent grid: as many CTAs as fit at once, at most one per work item.
   long long grid = (long long)num_sms * per_sm[dev].load(std::memory_order_relaxed);
   if (grid > params.total_items) grid = params.total_items;
   if (grid < 1) return cudaSuccess;
+  DecodeParams prm = params;
+  if (prm.trace != nullptr &&
+      (size_t)grid * 3 * (size_t)prm.trace_per_role * 16 > (size_t)prm.trace_bytes)
+    prm.trace = nullptr;  // the buffer cannot hold this launch's timeline
   paged_decode_tc_kernel<D, GP><<<(unsigned)grid, kTcThreads, smem_bytes, stream>>>(kv_map, q_map,
-                                                                                   params);
+                                                                                   prm);
   return cudaGetLastError();
 }
 

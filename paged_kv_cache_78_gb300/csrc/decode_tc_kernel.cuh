@@ -45,6 +45,7 @@ constexpr int kTcHeads = 16;     // N of both MMAs: query heads, G padded
 constexpr int kTcThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr int kTcTmemCols = 64;  // S x2, O x2, 16 columns each
 constexpr int kTcItemRing = 4;
+constexpr int kTcLensCache = 512;  // batches up to this size keep seq_lens in shared memory
 
 // Kinds of ring entries.
 constexpr int kItemAttend = 0;  // attention over tokens [tok0, tok1)
@@ -65,6 +66,7 @@ struct TcSmem {
   int item_off;  // item ring
   int bar_off;
   int misc_off;
+  int lens_off;  // cached sequence lengths (batches of up to kTcLensCache)
   int total;     // bytes to request (includes 1024 of alignment slack)
 };
 
@@ -81,7 +83,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages) 
   // full[NS], empty[NS], s/p/o full/free and q full/free [2 each], item
   // full/free [ring], drain
   l.misc_off = l.bar_off + 8 * (2 * num_stages + 14 + 2 * kTcItemRing + 1);
-  l.total = l.misc_off + 64 + 1024;
+  l.lens_off = l.misc_off + 64;
+  l.total = l.lens_off + kTcLensCache * 4 + 1024;
   return l;
 }
 
@@ -136,6 +139,26 @@ struct TcBars {
     drain = it_free + 8u * kTcItemRing;
   }
 };
+
+// One event of the optional timeline (see pa_set_decode_trace).
+__device__ __forceinline__ void tc_trace(const DecodeParams& p, int role, int& n, uint32_t tag,
+                                         uint32_t arg) {
+  if (p.trace != nullptr) {
+    if (n < p.trace_per_role) {
+      unsigned long long* e =
+          p.trace + (((size_t)blockIdx.x * 3 + role) * (size_t)p.trace_per_role + n) * 2;
+      e[0] = (unsigned long long)clock64();
+      e[1] = ((unsigned long long)tag << 32) | arg;
+    }
+    ++n;
+  }
+}
+
+__device__ __forceinline__ unsigned long long global_timer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Softmax warpgroup: add the PV tile of global stage gk (tensor-memory buffer
 // gk % 2) into the fp32 accumulator, rescaled by that stage's factor.
@@ -229,6 +252,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&kv_map);
     tma_prefetch_desc(&q_map);
   }
+  // Sequence lengths in shared memory, so classifying a work item needs no
+  // global load.
+  int* lens_s = p.num_seqs <= kTcLensCache ? reinterpret_cast<int*>(base + lay.lens_off) : nullptr;
+  if (lens_s)
+    for (int i = tid; i < p.num_seqs; i += kTcThreads) lens_s[i] = p.seq_lens[i];
   // Both P^T tiles start at zero: the softmax writes only rows below GP.
   for (int i = tid; i < 2 * 2 * kTcHeads * 128 / 16; i += kTcThreads)
     st_shared_zero16(p_s + (uint32_t)i * 16u);
@@ -248,7 +276,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t box_bytes = (uint32_t)R * 128u;
     const int sh = p.num_seqs * p.num_kv_heads;
     const int P = p.partition_tokens;
-    int gk = 0, qi = 0, ii = 0;
+    int gk = 0, qi = 0, ii = 0, ntr = 0;
+    if (lane == 0) tc_trace(p, 0, ntr, 9, p.trace ? (uint32_t)global_timer() : 0u);
     unsigned int idx = lane == 0 ? atomicAdd(p.sched, 1u) : 0u;
     while (true) {
       if (flags[0]) break;
@@ -260,7 +289,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int rem = (int)(idx % (unsigned)sh);
         it.s = rem / p.num_kv_heads;
         it.h = rem - it.s * p.num_kv_heads;
-        const int L = p.seq_lens[it.s];
+        const int L = lens_s ? lens_s[it.s] : p.seq_lens[it.s];
         const int nparts = L <= 0 ? 0 : (P > 0 ? (L + P - 1) / P : 1);
         if (L <= 0) {
           it.kind = kItemZero;
@@ -308,6 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ring[j].final_out = it.final_out;
           ring[j].kind = it.kind;
           mbar_arrive(bars.it_full + 8u * j);
+          tc_trace(p, 0, ntr, 1, (uint32_t)ii);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -316,7 +346,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       ++ii;
-      if (it.kind == kItemEnd) break;
+      if (it.kind == kItemEnd) {
+        if (lane == 0) tc_trace(p, 0, ntr, 8, (uint32_t)ii);
+        break;
+      }
       if (lane == 0) idx = atomicAdd(p.sched, 1u);  // next item, fetched early
       if (it.kind != kItemAttend) continue;
 
@@ -396,7 +429,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_5d(dst, &kv_map, bars.full0 + 8u * slot, 0, g, it.h, tk & (BS - 1), c4);
           }
         }
-        if (lane == 0) flags[1] = gk + 1;
+        if (lane == 0) {
+          flags[1] = gk + 1;
+          tc_trace(p, 0, ntr, 2, (uint32_t)gk);
+        }
       }
       if (!ok) {
         flags[0] = 1;
@@ -413,6 +449,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int next_qk = 0, next_pv = 0;  // global stage counters
       int ii = 0, qi = 0, qb = 0, qk_k = 0, qk_n = 0;
       bool have_item = false, need_q = false, end_seen = false, ok = true;
+      int ntr = 0;
       long long t_idle = clock64();
       while (true) {
         bool progress = false;
@@ -457,6 +494,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc::mma_bf16(tS0 + 16u * sb, a, bd, kIdescQK, kk > 0);
             }
             tc::mma_commit(bars.s_full + 8u * sb);
+            tc_trace(p, 1, ntr, 3, (uint32_t)gk);
             ++next_qk;
             if (++qk_k == qk_n) {
               tc::mma_commit(bars.q_free + 8u * qb);  // the item's Q tile is no longer read
@@ -484,6 +522,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc::mma_commit(bars.o_full + 8u * sb);
             tc::mma_commit(bars.empty0 + 8u * slot);
+            tc_trace(p, 1, ntr, 4, (uint32_t)gk);
             ++next_pv;
             progress = true;
           }
@@ -492,9 +531,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (progress) {
           t_idle = clock64();
         } else if (!flags[0]) {
-          // Nothing ready: back off instead of spinning, leaving issue slots
-          // to the softmax warp that shares this warp's scheduler.
-          __nanosleep(64);
+          // Nothing ready: suspend briefly (128 ns at most) on the barrier most
+          // likely to unblock this loop (the oldest pending PV's P tile, else
+          // the next QK's stage); it wakes early when that barrier completes,
+          // and leaves issue slots to the softmax warp sharing its scheduler.
+          if (next_pv < next_qk)
+            mbar_suspend(bars.p_full + 8u * (next_pv & 1), (next_pv >> 1) & 1, 128);
+          else if (have_item && !need_q)
+            mbar_suspend(bars.full0 + 8u * (next_qk % NS), (next_qk / NS) & 1, 128);
+          else if (have_item)
+            mbar_suspend(bars.q_full + 8u * qb, (qi >> 1) & 1, 128);
+          else if (!end_seen)
+            mbar_suspend(bars.it_full + 8u * (ii % kTcItemRing), (ii / kTcItemRing) & 1, 128);
         }
         if (progress) {
         } else if (flags[0]) {
@@ -520,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     const uint32_t tO_lane = tO0 + lane_addr;
     float* red2 = red + 2 * 4 * kTcHeads;
-    int gk = 0;
+    int gk = 0, ntr = 0;
     bool ok = true;
     for (int ii = 0;; ++ii) {
       const int j = ii % kTcItemRing;
@@ -567,6 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::tmem_wait_ld();
         tc::fence_before_sync();
         mbar_arrive(bars.s_free + 8u * sb);
+        if (tid == 64) tc_trace(p, 2, ntr, 5, (uint32_t)g_k);
 
         const int nvalid = min(kTcTokens, it.tok1 - (it.tok0 + k * kTcTokens));
         const bool valid = row < nvalid;
@@ -622,6 +671,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_proxy_async_smem();
         mbar_arrive(bars.p_full + 8u * sb);
+        if (tid == 64) tc_trace(p, 2, ntr, 6, (uint32_t)g_k);
         if (k >= 1) ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, o_acc, alpha_prev) && ok;
 #pragma unroll
         for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
@@ -657,6 +707,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      if (tid == 64) tc_trace(p, 2, ntr, 7, (uint32_t)ii);
     }
     if (!ok) flags[0] = 1;
   }

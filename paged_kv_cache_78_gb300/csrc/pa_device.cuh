@@ -69,6 +69,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Suspend until the phase with the given parity completes or about `ns`
+// nanoseconds pass, whichever comes first (the result is not reported).
+__device__ __forceinline__ void mbar_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%0], %1, %2;\n\t}" ::"r"(bar),
+      "r"(parity), "r"(ns)
+      : "memory");
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (and records PA_DEVERR_TIMEOUT) if that takes longer than kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
