@@ -171,6 +171,16 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
                        int32_t max_seq_len, int32_t partition_size, void* workspace,
                        size_t workspace_bytes, int32_t kernel, void* stream);
 
+/* The kernel family pa_decode_ex(..., kernel, ...) runs for a cache `desc`,
+ * num_seqs sequences of num_heads query heads and a query buffer at `query`
+ * (its address only decides the 16-byte alignment the tensor-core kernel
+ * needs; it is not read): PA_KERNEL_SIMT or PA_KERNEL_TENSOR in *selected.
+ * PA_ERR_UNSUPPORTED when the requested family has no kernel for these
+ * arguments, PA_ERR_INVALID_ARG for arguments pa_decode_ex rejects.  Host
+ * only: touches no device. */
+pa_status pa_decode_select_kernel(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_heads,
+                                  const void* query, int32_t kernel, int32_t* selected);
+
 /* The partition size pa_decode uses for these arguments (0 = no split). */
 pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t num_heads, int32_t max_seq_len,
@@ -294,17 +304,23 @@ const char* pa_status_string(pa_status status);
 
 /* Timeline of the tensor-core decode, for performance work.  After a call
  * with a non-NULL device buffer, every tensor-core pa_decode of this process
- * records, per CTA and per role (0 producer, 1 MMA issuer, 2 softmax
- * warpgroup), its first events_per_role events as two 64-bit words
- *     buf[((cta * 3 + role) * events_per_role + i) * 2 + 0] = SM clock (clock64)
- *     buf[((cta * 3 + role) * events_per_role + i) * 2 + 1] = tag << 32 | argument
- * Tags (argument): 1 item published (item number), 2 stage loads issued
- * (stage), 3 QK issued (stage), 4 PV issued (stage), 5 scores read (stage),
- * 6 P written (stage), 7 item output written (item number), 8 producer done
- * (items), 9 CTA start (low 32 bits of the global timer, ns).  Entries
- * beyond a role's events are left as they were.  A launch whose grid needs
- * more than `bytes` records nothing.  NULL turns tracing off (the default).
- * Host-side setting shared by all threads of the process. */
+ * records, per CTA and per warp (0 producer, 1 MMA issuer, 2..5 softmax
+ * warpgroup), the warp's first events_per_role events as two 64-bit words
+ *     buf[((cta * 6 + warp) * events_per_role + i) * 2 + 0] = SM clock (clock64)
+ *     buf[((cta * 6 + warp) * events_per_role + i) * 2 + 1] = tag << 32 | argument
+ * Tags (argument), producer: 9 CTA start (low 32 bits of the global timer,
+ * ns), 10 work item classified (item index), 1 item published (item
+ * number), 11 query tile issued (count), 12 block-table window loaded,
+ * 20 stage's boxes about to be issued (stage), 2 stage's boxes issued
+ * (stage), 8 producer done (items).  MMA issuer: 13 item taken (item
+ * number), 3 QK issued (stage), 17 P.V inputs ready (stage), 4 PV issued
+ * (stage).  Softmax warp 2: 14 item taken (item number), 15 scores ready
+ * (stage), 5 scores read (stage), 6 P written (stage), 16 stage's P.V added
+ * (stage), 7 item output written (item number); warps 3..5: 19 P written
+ * (warp << 16 | stage).  Entries beyond a warp's events are left as they
+ * were.  A launch whose grid needs more than `bytes` records nothing.  NULL
+ * turns tracing off (the default).  Host-side setting shared by all threads
+ * of the process. */
 pa_status pa_set_decode_trace(void* device_buffer, size_t bytes, int32_t events_per_role);
 /* Library version, e.g. "0.1.0". */
 const char* pa_version(void);

@@ -40,7 +40,7 @@ PA_DEVERR_TIMEOUT = 0x8
 # Every function include/pa.h declares.
 EXPORTS = (
     "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_no_alloc",
-    "pa_decode_partition_size",
+    "pa_decode_partition_size", "pa_decode_select_kernel",
     "pa_decode_workspace_size", "pa_slot_mapping", "pa_pool_create", "pa_pool_destroy",
     "pa_pool_add_seq", "pa_pool_fork", "pa_pool_append_token", "pa_pool_append_tokens",
     "pa_pool_free_seq", "pa_pool_block_table", "pa_pool_fill_tables", "pa_pool_slot",
@@ -81,6 +81,7 @@ def _load() -> ctypes.CDLL:
         "pa_decode_ex": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, i32, vp],
         "pa_decode_no_alloc": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp],
         "pa_decode_partition_size": [desc, i32, i32, i32, i32, p_i32],
+        "pa_decode_select_kernel": [desc, i32, i32, vp, i32, p_i32],
         "pa_decode_workspace_size": [desc, i32, i32, i32, i32, p_sz],
         "pa_slot_mapping": [vp, i32, i32, i32, i32, vp, vp, i32, vp],
         "pa_pool_create": [i32, i32, vp, ctypes.POINTER(vp)],
@@ -210,6 +211,20 @@ def pa_decode_partition_size(cache_or_desc, num_seqs: int, num_heads: int, max_s
     _check(lib.pa_decode_partition_size(ctypes.byref(desc), num_seqs, num_heads, max_seq_len,
                                         partition_size, ctypes.byref(out)),
            "pa_decode_partition_size")
+    return out.value
+
+
+def pa_decode_select_kernel(cache_or_desc, num_seqs: int, num_heads: int, query_ptr: int = 0,
+                            kernel: int = 0) -> int:
+    """The kernel family (PA_KERNEL_SIMT or PA_KERNEL_TENSOR) pa_decode runs
+    for these arguments; `query_ptr` is the query's device address (only its
+    alignment matters), or 0 to assume a 256-byte aligned buffer."""
+    desc = cache_or_desc if isinstance(cache_or_desc, CacheDesc) else cache_desc(cache_or_desc)
+    out = ctypes.c_int32()
+    _check(lib.pa_decode_select_kernel(ctypes.byref(desc), num_seqs, num_heads,
+                                       ctypes.c_void_p(query_ptr or 256), kernel,
+                                       ctypes.byref(out)),
+           "pa_decode_select_kernel")
     return out.value
 
 
@@ -399,9 +414,13 @@ class Pool:
 
 def tensor_core_supported(cache: torch.Tensor, num_heads: int) -> bool:
     """Whether PA_KERNEL_TENSOR has a kernel for this cache and head count."""
-    d = cache_desc(cache)
-    g = num_heads // d.num_kv_heads
-    return d.dtype == PA_BF16 and d.head_size in (64, 128) and g <= 16 and d.block_size >= 8
+    try:
+        pa_decode_select_kernel(cache, 1, num_heads, kernel=PA_KERNEL_TENSOR)
+    except PAError as e:
+        if e.status == PA_ERR_UNSUPPORTED:
+            return False
+        raise
+    return True
 
 
 def pa_set_decode_trace(buffer: torch.Tensor | None, events_per_role: int = 0) -> None:

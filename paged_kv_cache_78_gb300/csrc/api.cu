@@ -136,6 +136,35 @@ size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_p
          (rows * 4 + 255) / 256 * 256;
 }
 
+// The kernel family for a decode call (desc already checked).
+pa_status select_kernel(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_heads,
+                        const void* query, int32_t kernel, int32_t* selected) {
+  const int group = num_heads / desc->num_kv_heads;
+  const int D = desc->head_size;
+  if (!head_size_supported(D) || desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  // Tensor cores: bf16, head size 64 or 128, query group up to 16, blocks of
+  // at least 8 tokens (a TMA box then fills whole 1024-byte swizzle atoms).
+  const bool tc_ok = desc->dtype == PA_BF16 && (D == 64 || D == 128) && group <= pa::kTcHeads &&
+                     desc->block_size >= 8 && aligned(query, 16) &&
+                     (long long)num_seqs * num_heads < (1ll << 31) &&
+                     (long long)desc->num_blocks * (desc->block_size / 8) < (1ll << 31);
+  bool use_tc;
+  if (kernel == PA_KERNEL_TENSOR) {
+    if (!tc_ok) return PA_ERR_UNSUPPORTED;
+    use_tc = true;
+  } else if (kernel == PA_KERNEL_SIMT) {
+    use_tc = false;
+  } else {
+    // Automatic choice: the tensor-core kernel for grouped queries (G >= 2),
+    // whose CUDA-core cost grows with G; the CUDA-core kernel for G = 1,
+    // where it measures faster.
+    use_tc = tc_ok && group >= 2;
+  }
+  if (!use_tc && group > 8) return PA_ERR_UNSUPPORTED;
+  *selected = use_tc ? PA_KERNEL_TENSOR : PA_KERNEL_SIMT;
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,6 +276,17 @@ pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
   return PA_OK;
 }
 
+pa_status pa_decode_select_kernel(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_heads,
+                                  const void* query, int32_t kernel, int32_t* selected) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (!selected || num_seqs < 0 || num_heads < 1 || num_heads % desc->num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_SIMT && kernel != PA_KERNEL_TENSOR)
+    return PA_ERR_INVALID_ARG;
+  return select_kernel(desc, num_seqs, num_heads, query, kernel, selected);
+}
+
 pa_status pa_decode(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
                     const int32_t* block_tables, int32_t max_blocks_per_seq,
                     const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
@@ -279,24 +319,9 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   const int group = num_heads / desc->num_kv_heads;
   const int D = desc->head_size;
   const int BS = desc->block_size;
-  if (!head_size_supported(D) || desc->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
-  // Tensor cores: bf16, head size 64 or 128, query group up to 16, blocks of
-  // at least 8 tokens (a TMA box then fills whole 1024-byte swizzle atoms).
-  const bool tc_ok = desc->dtype == PA_BF16 && (D == 64 || D == 128) && group <= pa::kTcHeads &&
-                     BS >= 8 && aligned(query, 16) && (long long)num_seqs * num_heads < (1ll << 31);
-  bool use_tc;
-  if (kernel == PA_KERNEL_TENSOR) {
-    if (!tc_ok) return PA_ERR_UNSUPPORTED;
-    use_tc = true;
-  } else if (kernel == PA_KERNEL_SIMT) {
-    use_tc = false;
-  } else {
-    // Automatic choice: the tensor-core kernel for grouped queries (G >= 2),
-    // whose CUDA-core cost grows with G; the CUDA-core kernel for G = 1,
-    // where it measures faster.
-    use_tc = tc_ok && group >= 2;
-  }
-  if (!use_tc && group > 8) return PA_ERR_UNSUPPORTED;
+  int32_t family = 0;
+  if ((st = select_kernel(desc, num_seqs, num_heads, query, kernel, &family)) != PA_OK) return st;
+  const bool use_tc = family == PA_KERNEL_TENSOR;
 
   unsigned int* err = nullptr;
   int sms = 0;
@@ -384,12 +409,30 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
                                  (cuuint64_t)BS * desc->num_kv_heads * D * es};
   const cuuint32_t box[5] = {(cuuint32_t)inner, 1u, 1u, (cuuint32_t)R, 1u};
   const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
-  CUresult cr = encode(&map,
-                       desc->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                       5, const_cast<void*>(cache), gdim, gstride, box, estride,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult cr;
+  if (use_tc) {
+    // The tensor-core kernel's map puts one block's K and V rows, every
+    // 128-byte column group, in one box, laid out per 8-token chunk as
+    // [column group][K rows][V rows] (each 8 rows one 1024-byte swizzle
+    // atom).  Dimensions, innermost first: 64 elements; token within an
+    // 8-token chunk; K or V; (KV head, column group); 8-token chunk of the
+    // plane (block * block_size / 8 + chunk within the block).
+    const cuuint64_t row = (cuuint64_t)desc->num_kv_heads * D * es;
+    const cuuint64_t tdim[5] = {64ull, 8ull, 2ull, (cuuint64_t)desc->num_kv_heads * (D / 64),
+                                (cuuint64_t)desc->num_blocks * (cuuint64_t)(BS / 8)};
+    const cuuint64_t tstride[4] = {row, (cuuint64_t)desc->num_blocks * BS * row, 128ull, 8 * row};
+    const cuuint32_t tbox[5] = {64u, 8u, 2u, (cuuint32_t)(D / 64), (cuuint32_t)(R / 8)};
+    cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), tdim,
+                tstride, tbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cr = encode(&map,
+                desc->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                5, const_cast<void*>(cache), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (cr != CUDA_SUCCESS) return PA_ERR_CUDA;
   // The tensor-core kernel loads each work item's 16 query rows by TMA: the
   // queries as [rows = num_seqs * num_heads][column group][64 elements].

@@ -21,6 +21,8 @@ __global__ void reshape_and_cache_kernel(uint8_t* __restrict__ cache,
                                          const int64_t* __restrict__ slot_mapping,
                                          int64_t num_tokens, int64_t num_slots, int row_chunks,
                                          int64_t plane_bytes, unsigned int* err) {
+  grid_dependents_launch();
+  grid_dependency_wait();
   const int64_t per_token = 2 * (int64_t)row_chunks;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= num_tokens * per_token) return;
@@ -46,6 +48,8 @@ __global__ void reshape_and_cache_kernel(uint8_t* __restrict__ cache,
 __global__ void copy_blocks_kernel(uint8_t* __restrict__ cache, const int64_t* __restrict__ pairs,
                                    int64_t num_blocks, int64_t block_bytes, int64_t plane_bytes,
                                    unsigned int* err) {
+  grid_dependents_launch();
+  grid_dependency_wait();
   const int pair = blockIdx.x >> 1;
   const int kv = blockIdx.x & 1;
   const int64_t src = __ldg(pairs + 2 * pair);
@@ -81,11 +85,13 @@ cudaError_t launch_reshape_and_cache(void* cache, const void* key, const void* v
   const int64_t threads = num_tokens * 2 * row_chunks;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
-  reshape_and_cache_kernel<<<(unsigned)grid, block, 0, stream>>>(
-      static_cast<uint8_t*>(cache), static_cast<const uint8_t*>(key),
-      static_cast<const uint8_t*>(value), slot_mapping, num_tokens, num_slots, row_chunks,
-      plane_bytes, err);
-  return cudaGetLastError();
+  uint8_t* c = static_cast<uint8_t*>(cache);
+  const uint8_t* k = static_cast<const uint8_t*>(key);
+  const uint8_t* v = static_cast<const uint8_t*>(value);
+  void* args[] = {&c, &k, &v, &slot_mapping, &num_tokens, &num_slots,
+                  const_cast<int*>(&row_chunks), &plane_bytes, &err};
+  return launch_overlapped((const void*)reshape_and_cache_kernel, dim3((unsigned)grid),
+                           dim3(block), 0, stream, args);
 }
 
 cudaError_t launch_copy_blocks(void* cache, const int64_t* pairs, int num_pairs,
@@ -97,9 +103,9 @@ cudaError_t launch_copy_blocks(void* cache, const int64_t* pairs, int num_pairs,
   if (slices < 1) slices = 1;
   if (slices > 1024) slices = 1024;
   dim3 grid((unsigned)num_pairs * 2u, (unsigned)slices);
-  copy_blocks_kernel<<<grid, block, 0, stream>>>(static_cast<uint8_t*>(cache), pairs,
-                                                 num_blocks, block_bytes, plane_bytes, err);
-  return cudaGetLastError();
+  uint8_t* c = static_cast<uint8_t*>(cache);
+  void* args[] = {&c, &pairs, &num_blocks, &block_bytes, &plane_bytes, &err};
+  return launch_overlapped((const void*)copy_blocks_kernel, grid, dim3(block), 0, stream, args);
 }
 
 }  // namespace pa

@@ -25,8 +25,9 @@ cudaError_t launch_decode_one(dim3 grid, int smem_bytes, cudaStream_t stream,
     if (e != cudaSuccess) return e;
     configured[dev].store(smem_bytes, std::memory_order_relaxed);
   }
-  paged_decode_kernel<T, D, G><<<grid, kDecodeThreads, smem_bytes, stream>>>(map, params);
-  return cudaGetLastError();
+  void* args[] = {const_cast<CUtensorMap*>(&map), const_cast<DecodeParams*>(&params)};
+  return launch_overlapped((const void*)paged_decode_kernel<T, D, G>, grid, dim3(kDecodeThreads),
+                           (size_t)smem_bytes, stream, args);
 }
 
 template <typename T, int D>
@@ -53,9 +54,9 @@ cudaError_t launch_reduce_for_head_size(void* out, const float* part_o, const fl
                                         int partition_tokens, int max_parts,
                                         cudaStream_t stream) {
   dim3 grid((unsigned)num_heads, (unsigned)num_seqs);
-  lse_reduce_kernel<T, D><<<grid, D, 0, stream>>>(out, part_o, part_lse, seq_lens, num_heads,
-                                                  partition_tokens, max_parts);
-  return cudaGetLastError();
+  void* args[] = {&out, &part_o, &part_lse, &seq_lens, &num_heads, &partition_tokens, &max_parts};
+  return launch_overlapped((const void*)lse_reduce_kernel<T, D>, grid, dim3(kReduceThreads), 0,
+                           stream, args);
 }
 
 }  // namespace pa

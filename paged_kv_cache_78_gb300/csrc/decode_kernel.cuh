@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
+  grid_dependency_wait();
   const int L = p.seq_lens[s];
   const int P = p.partition_tokens;
   const bool split = P > 0;
@@ -440,31 +441,103 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
 // Log-sum-exp combination of split-KV partials:
 //   M = max_p lse_p,  w_p = 2^(lse_p - M),  out = sum_p w_p o_p / sum_p w_p.
-// One CTA per (query head, sequence); one thread per output element.
+// One CTA per (query head, sequence).  Its threads split the partitions into
+// kReduceThreads / (D / 4) slices, each thread summing float4 columns of its
+// slice's partials (four loads in flight); the slices are then added through
+// shared memory.  The weights of up to kReduceChunk partitions at a time are
+// staged in shared memory.
+constexpr int kReduceThreads = 256;
+constexpr int kReduceChunk = 1024;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kReduceThreads, 4)
     lse_reduce_kernel(void* out_, const float* __restrict__ part_o,
                       const float* __restrict__ part_lse, const int32_t* __restrict__ seq_lens,
                       int num_heads, int partition_tokens, int max_parts) {
   using E = ElemTraits<T>;
+  constexpr int kCols = D / 4;                      // float4 columns of a row
+  constexpr int kSlices = kReduceThreads / kCols;   // partitions summed in parallel
+  static_assert(kReduceThreads % kCols == 0 && kSlices >= 1, "reduce shape");
+  __shared__ float w_s[kReduceChunk];
+  __shared__ __align__(16) float acc_s[kSlices][D];
+  __shared__ float red_s[kReduceThreads / 32];
+  __shared__ float bcast_s;
+
   const int hq = blockIdx.x;
   const int s = blockIdx.y;
-  const int d = threadIdx.x;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  grid_dependency_wait();
   const int L = seq_lens[s];
   const int nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
   if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
   const size_t row = (size_t)s * num_heads + hq;
   const float* lse = part_lse + row * max_parts;
-  const float* po = part_o + row * max_parts * D;
-  float M = -INFINITY;
-  for (int q = 0; q < nparts; ++q) M = fmaxf(M, lse[q]);
-  float wsum = 0.f, acc = 0.f;
-  for (int q = 0; q < nparts; ++q) {
-    const float w = fast_exp2(lse[q] - M);
-    wsum += w;
-    acc = fmaf(w, po[(size_t)q * D + d], acc);
+  const float4* po = reinterpret_cast<const float4*>(part_o + row * max_parts * D);
+
+  // M over the row's partitions.
+  float m = -INFINITY;
+  for (int q = tid; q < nparts; q += kReduceThreads) m = fmaxf(m, lse[q]);
+  m = warp_max(m);
+  if (lane == 0) red_s[warp] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float v = red_s[0];
+    for (int i = 1; i < kReduceThreads / 32; ++i) v = fmaxf(v, red_s[i]);
+    bcast_s = v;
   }
-  reinterpret_cast<T*>(out_)[row * D + d] = E::from_float(acc / wsum);
+  __syncthreads();
+  const float M = bcast_s;
+
+  const int col = tid % kCols;
+  const int slice = tid / kCols;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int c0 = 0; c0 < nparts; c0 += kReduceChunk) {
+    const int cn = min(kReduceChunk, nparts - c0);
+    if (c0 > 0) __syncthreads();  // the previous chunk's weights are consumed
+    for (int q = tid; q < cn; q += kReduceThreads) {
+      const float w = fast_exp2(lse[c0 + q] - M);
+      w_s[q] = w;
+      wsum += w;
+    }
+    __syncthreads();
+    int q = slice;
+    for (; q + 3 * kSlices < cn; q += 4 * kSlices) {
+      const float4 a = po[(size_t)(c0 + q) * kCols + col];
+      const float4 b = po[(size_t)(c0 + q + kSlices) * kCols + col];
+      const float4 c = po[(size_t)(c0 + q + 2 * kSlices) * kCols + col];
+      const float4 d = po[(size_t)(c0 + q + 3 * kSlices) * kCols + col];
+      const float wa = w_s[q], wb = w_s[q + kSlices], wc = w_s[q + 2 * kSlices],
+                  wd = w_s[q + 3 * kSlices];
+      acc.x = fmaf(wa, a.x, acc.x); acc.y = fmaf(wa, a.y, acc.y);
+      acc.z = fmaf(wa, a.z, acc.z); acc.w = fmaf(wa, a.w, acc.w);
+      acc.x = fmaf(wb, b.x, acc.x); acc.y = fmaf(wb, b.y, acc.y);
+      acc.z = fmaf(wb, b.z, acc.z); acc.w = fmaf(wb, b.w, acc.w);
+      acc.x = fmaf(wc, c.x, acc.x); acc.y = fmaf(wc, c.y, acc.y);
+      acc.z = fmaf(wc, c.z, acc.z); acc.w = fmaf(wc, c.w, acc.w);
+      acc.x = fmaf(wd, d.x, acc.x); acc.y = fmaf(wd, d.y, acc.y);
+      acc.z = fmaf(wd, d.z, acc.z); acc.w = fmaf(wd, d.w, acc.w);
+    }
+    for (; q < cn; q += kSlices) {
+      const float4 a = po[(size_t)(c0 + q) * kCols + col];
+      const float wa = w_s[q];
+      acc.x = fmaf(wa, a.x, acc.x); acc.y = fmaf(wa, a.y, acc.y);
+      acc.z = fmaf(wa, a.z, acc.z); acc.w = fmaf(wa, a.w, acc.w);
+    }
+  }
+  reinterpret_cast<float4*>(&acc_s[slice][0])[col] = acc;
+  wsum = warp_sum(wsum);
+  if (lane == 0) red_s[warp] = wsum;
+  __syncthreads();
+  if (tid < D) {
+    float ws = 0.f;
+    for (int i = 0; i < kReduceThreads / 32; ++i) ws += red_s[i];
+    float v = 0.f;
+    for (int i = 0; i < kSlices; ++i) v += acc_s[i][tid];
+    reinterpret_cast<T*>(out_)[row * D + tid] = E::from_float(v / ws);
+  }
 }
 
 }  // namespace pa

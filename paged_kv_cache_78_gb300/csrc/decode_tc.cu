@@ -49,11 +49,11 @@ static cudaError_t launch_tc(int num_sms, int smem_bytes, cudaStream_t stream,
   if (grid < 1) return cudaSuccess;
   DecodeParams prm = params;
   if (prm.trace != nullptr &&
-      (size_t)grid * 3 * (size_t)prm.trace_per_role * 16 > (size_t)prm.trace_bytes)
+      (size_t)grid * kTcTraceRoles * (size_t)prm.trace_per_role * 16 > (size_t)prm.trace_bytes)
     prm.trace = nullptr;  // the buffer cannot hold this launch's timeline
-  paged_decode_tc_kernel<D, GP><<<(unsigned)grid, kTcThreads, smem_bytes, stream>>>(kv_map, q_map,
-                                                                                   prm);
-  return cudaGetLastError();
+  void* args[] = {const_cast<CUtensorMap*>(&kv_map), const_cast<CUtensorMap*>(&q_map), &prm};
+  return launch_overlapped((const void*)paged_decode_tc_kernel<D, GP>, dim3((unsigned)grid),
+                           dim3(kTcThreads), (size_t)smem_bytes, stream, args);
 }
 
 template <int D>

@@ -17,9 +17,10 @@
 //   warp 0      producer: takes the next item, publishes it in a 4-entry ring,
 //               loads the item's 16 query rows by TMA straight into the
 //               swizzled B-operand layout, and streams the item's 128-token
-//               K/V stages (one TMA box per block, 128-byte column group and
-//               K or V, in the 128-byte swizzle the MMA descriptors read),
-//               the boxes of a stage issued by all 32 lanes at once;
+//               K/V stages, one TMA box per block holding the block's K and V
+//               rows of every column group (in the 128-byte swizzle the MMA
+//               descriptors read), the boxes of a stage issued by all 32
+//               lanes at once;
 //   warp 1      tensor-memory allocator and MMA issuer (one thread), an event
 //               loop that issues QK (up to two stages ahead) and PV (in order)
 //               as soon as each one's inputs are ready;
@@ -46,6 +47,7 @@ constexpr int kTcThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr int kTcTmemCols = 64;  // S x2, O x2, 16 columns each
 constexpr int kTcItemRing = 4;
 constexpr int kTcLensCache = 512;  // batches up to this size keep seq_lens in shared memory
+constexpr int kTcTraceRoles = 6;   // timeline regions per CTA: one per warp
 
 // Kinds of ring entries.
 constexpr int kItemAttend = 0;  // attention over tokens [tok0, tok1)
@@ -146,7 +148,7 @@ __device__ __forceinline__ void tc_trace(const DecodeParams& p, int role, int& n
   if (p.trace != nullptr) {
     if (n < p.trace_per_role) {
       unsigned long long* e =
-          p.trace + (((size_t)blockIdx.x * 3 + role) * (size_t)p.trace_per_role + n) * 2;
+          p.trace + (((size_t)blockIdx.x * kTcTraceRoles + role) * (size_t)p.trace_per_role + n) * 2;
       e[0] = (unsigned long long)clock64();
       e[1] = ((unsigned long long)tag << 32) | arg;
     }
@@ -189,8 +191,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(D == 64 || D == 128, "tensor-core decode handles head sizes 64 and 128");
   static_assert(GP >= 1 && GP <= kTcHeads && (GP & (GP - 1)) == 0, "padded group");
   constexpr int kGroups = D / 64;                 // 128-byte column groups of a row
-  constexpr int kGroupBytes = kTcTokens * 128;    // one column group of a 128-token tile
-  constexpr int kRegion = kGroups * kGroupBytes;  // K (or V) tile of a stage
+  // A stage holds 16 chunks of 8 tokens; a chunk holds, per column group, the
+  // group's 8 K rows (1024 bytes, one 128-byte swizzle atom) then its 8 V rows.
+  constexpr int kChunkBytes = kGroups * 2048;
   constexpr int kQTile = kGroups * kTcHeads * 128;
   constexpr int kKSteps = D / 16;                 // QK: K = head dimension
   constexpr int kPvSteps = kTcTokens / 16;        // PV: K = tokens
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, kTcHeads, 1);
   // PV's A operand (V^T) spans 128 rows = two 64-dimension groups; with one
   // group (D = 64) both halves read the same group and rows 64..127 repeat.
-  constexpr uint32_t kPvLbo = kGroups > 1 ? kGroupBytes : 0;
+  constexpr uint32_t kPvLbo = kGroups > 1 ? 2048 : 0;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -252,14 +255,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&kv_map);
     tma_prefetch_desc(&q_map);
   }
+  // Both P^T tiles start at zero: the softmax writes only rows below GP.
+  for (int i = tid; i < 2 * 2 * kTcHeads * 128 / 16; i += kTcThreads)
+    st_shared_zero16(p_s + (uint32_t)i * 16u);
+  // Everything above touches only this CTA's own resources and may overlap
+  // the previous kernel; from here on global memory is read.  The next
+  // kernel (the split-KV reduce) may start launching: this grid is resident
+  // as a whole, so its CTAs only take room this grid does not use.
+  grid_dependency_wait();
+  grid_dependents_launch();
+  // The first work item of CTA b is item b (later ones come from the work
+  // counter); the producer loads its block-table window now, overlapping the
+  // sequence-length loads below.
+  int pf_win = -1, pf_s = -1, pf_cur = 0, pf_nxt = 0;
+  if (warp == 0 && (int)blockIdx.x < p.total_items) {
+    const int sh = p.num_seqs * p.num_kv_heads;
+    const int part = (int)blockIdx.x / sh;
+    pf_s = ((int)blockIdx.x - part * sh) / p.num_kv_heads;
+    pf_win = (p.partition_tokens > 0 ? part * p.partition_tokens : 0) >> p.log2_block_size;
+    const int32_t* row = p.block_tables + (size_t)pf_s * p.max_blocks_per_seq;
+    pf_cur = pf_win + lane < p.max_blocks_per_seq ? __ldg(row + pf_win + lane) : 0;
+    pf_nxt = pf_win + 32 + lane < p.max_blocks_per_seq ? __ldg(row + pf_win + 32 + lane) : 0;
+  }
   // Sequence lengths in shared memory, so classifying a work item needs no
   // global load.
   int* lens_s = p.num_seqs <= kTcLensCache ? reinterpret_cast<int*>(base + lay.lens_off) : nullptr;
   if (lens_s)
     for (int i = tid; i < p.num_seqs; i += kTcThreads) lens_s[i] = p.seq_lens[i];
-  // Both P^T tiles start at zero: the softmax writes only rows below GP.
-  for (int i = tid; i < 2 * 2 * kTcHeads * 128 / 16; i += kTcThreads)
-    st_shared_zero16(p_s + (uint32_t)i * 16u);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
@@ -273,12 +295,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int l2bs = p.log2_block_size;
     const int R = p.box_rows;  // min(block_size, 128)
     const int log2R = p.log2_box_rows;
-    const uint32_t box_bytes = (uint32_t)R * 128u;
+    // A box = one block's rows (at most 128) of K and V, every column group.
+    const uint32_t box_bytes = (uint32_t)R * (uint32_t)kGroups * 256u;
+    const int chunks_per_block = BS >> 3;
     const int sh = p.num_seqs * p.num_kv_heads;
     const int P = p.partition_tokens;
     int gk = 0, qi = 0, ii = 0, ntr = 0;
     if (lane == 0) tc_trace(p, 0, ntr, 9, p.trace ? (uint32_t)global_timer() : 0u);
-    unsigned int idx = lane == 0 ? atomicAdd(p.sched, 1u) : 0u;
+    unsigned int idx = blockIdx.x;
     while (true) {
       if (flags[0]) break;
       // Lane 0 classifies the item; the warp follows its decision.
@@ -308,9 +332,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           it.final_out = nparts == 1;
         }
       }
+      if (lane == 0) tc_trace(p, 0, ntr, 10, idx);
       skip = __shfl_sync(0xffffffffu, skip, 0);
       if (skip) {
-        if (lane == 0) idx = atomicAdd(p.sched, 1u);
+        if (lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
         continue;
       }
       it.s = __shfl_sync(0xffffffffu, it.s, 0);
@@ -350,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) tc_trace(p, 0, ntr, 8, (uint32_t)ii);
         break;
       }
-      if (lane == 0) idx = atomicAdd(p.sched, 1u);  // next item, fetched early
+      if (lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
       if (it.kind != kItemAttend) continue;
 
       // Query rows h*G .. h*G+15 of sequence s (rows past G are masked).
@@ -372,7 +397,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       ++qi;
-      if (lane == 0) flags[2] = qi;
+      if (lane == 0) {
+        flags[2] = qi;
+        tc_trace(p, 0, ntr, 11, (uint32_t)qi);
+      }
 
       // The item's K/V stages.  Every lane issues TMA boxes (a box = one
       // block's rows of one 128-byte column group of K or of V): one thread
@@ -382,9 +410,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
       const int lb_end = (it.tok1 + BS - 1) >> l2bs;
       int win = it.tok0 >> l2bs;
-      int cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
-      int nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
-      constexpr int kOpsPerBox = kGroups * 2;
+      int cur, nxt;
+      if (win == pf_win && it.s == pf_s) {  // the first item's window, loaded early
+        cur = pf_cur;
+        nxt = pf_nxt;
+      } else {
+        cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
+        nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+      }
+      pf_win = -1;
+      if (lane == 0) tc_trace(p, 0, ntr, 12, (uint32_t)(cur + nxt));
       for (int k = 0; k < it.nstages; ++k, ++gk) {
         const int slot = gk % NS;
         if (gk >= NS) {
@@ -401,32 +436,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           win += 32;
           nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
         }
-        if (lane == 0)
-          mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)(nbox * kOpsPerBox) * box_bytes);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)nbox * box_bytes);
+          tc_trace(p, 0, ntr, 20, (uint32_t)gk);
+        }
         __syncwarp();
         const uint32_t kdst = sbase + (uint32_t)slot * (uint32_t)lay.stage;
-        const int nops = nbox * kOpsPerBox;
-        for (int b0 = 0; b0 < nops; b0 += 32) {
-          const int op = b0 + lane;
-          const bool live = op < nops;
-          const int i = live ? op / kOpsPerBox : 0;
-          const int r = op - i * kOpsPerBox;
-          const int tk = st_tok + (i << log2R);
+        for (int b0 = 0; b0 < nbox; b0 += 32) {
+          const int i = b0 + lane;
+          const bool live = i < nbox;
+          const int tk = st_tok + ((live ? i : 0) << log2R);
           const int src = (tk >> l2bs) - win;  // 0 .. 47
           const int id_cur = __shfl_sync(0xffffffffu, cur, src & 31);
           const int id_nxt = __shfl_sync(0xffffffffu, nxt, src & 31);
           if (live) {
             const int id = src < 32 ? id_cur : id_nxt;
-            const int g = r >> 1;
-            const int kv = r & 1;
-            int c4 = kv * p.num_blocks + id;
+            // 8-token chunk of the plane: block * (BS / 8) + chunk within the block.
+            int c4 = id * chunks_per_block + ((tk & (BS - 1)) >> 3);
             if (id < 0 || id >= p.num_blocks) {
               record_error(p.err, PA_DEVERR_BLOCK_ID);
-              c4 = 2 * p.num_blocks;  // outside the tensor: zero fill
+              c4 = p.num_blocks * chunks_per_block;  // outside the tensor: zero fill
             }
-            const uint32_t dst = kdst + (uint32_t)(kv * kRegion + g * kGroupBytes) +
-                                 (uint32_t)i * box_bytes;
-            tma_load_5d(dst, &kv_map, bars.full0 + 8u * slot, 0, g, it.h, tk & (BS - 1), c4);
+            tma_load_5d(kdst + (uint32_t)i * box_bytes, &kv_map, bars.full0 + 8u * slot, 0, 0, 0,
+                        it.h * kGroups, c4);
           }
         }
         if (lane == 0) {
@@ -459,6 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int kind = ring[j].kind;
             const int n = ring[j].nstages;
             mbar_arrive(bars.it_free + 8u * j);
+            tc_trace(p, 1, ntr, 13, (uint32_t)ii);
             ++ii;
             progress = true;
             if (kind == kItemEnd) {
@@ -476,6 +509,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           need_q = false;
           progress = true;
         }
+        if (next_pv < next_qk) {
+          const int gk = next_pv;
+          const int slot = gk % NS;
+          const int sb = gk & 1;
+          if (mbar_test(bars.p_full + 8u * sb, (gk >> 1) & 1) &&
+              (gk < 2 || mbar_test(bars.o_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+            tc_trace(p, 1, ntr, 17, (uint32_t)gk);
+            tc::fence_after_sync();
+            // A: the stage's V rows read MN-major (V^T), 64-dimension groups
+            // kPvLbo apart, 8-token groups kChunkBytes apart; B: P^T.
+            const uint64_t a0 = tc::smem_desc_sw128(
+                sbase + (uint32_t)slot * (uint32_t)lay.stage + 1024u, kPvLbo, kChunkBytes);
+            const uint64_t b0 = tc::smem_desc_sw128(p_s + (uint32_t)sb * 2u * kTcHeads * 128u, 16,
+                                                    1024);
+#pragma unroll
+            for (int kk = 0; kk < kPvSteps; ++kk) {
+              const uint32_t aoff = (uint32_t)(kk * 2 * kChunkBytes);
+              const uint32_t boff = (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32);
+              tc::mma_bf16(tO0 + 16u * sb, a0 + (aoff >> 4), b0 + (boff >> 4), kIdescPV, kk > 0);
+            }
+            tc::mma_commit(bars.o_full + 8u * sb);
+            tc::mma_commit(bars.empty0 + 8u * slot);
+            tc_trace(p, 1, ntr, 4, (uint32_t)gk);
+            ++next_pv;
+            progress = true;
+          }
+        }
         if (have_item && !need_q && next_qk < next_pv + 2) {
           const int gk = next_qk;
           const int slot = gk % NS;
@@ -483,15 +543,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (mbar_test(bars.full0 + 8u * slot, (gk / NS) & 1) &&
               (gk < 2 || mbar_test(bars.s_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
             tc::fence_after_sync();
-            const uint32_t ka = sbase + (uint32_t)slot * (uint32_t)lay.stage;
-            const uint32_t q_tile = q_s + (uint32_t)(qb * kQTile);
+            // A: the stage's K rows, K-major, 8-row groups kChunkBytes apart;
+            // B: the item's Q tile.  Descriptors advance by address / 16.
+            const uint64_t a0 = tc::smem_desc_sw128(sbase + (uint32_t)slot * (uint32_t)lay.stage,
+                                                    16, kChunkBytes);
+            const uint64_t b0 = tc::smem_desc_sw128(q_s + (uint32_t)(qb * kQTile), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kKSteps; ++kk) {
-              const uint32_t goff = (uint32_t)((kk >> 2) * kGroupBytes) + (uint32_t)((kk & 3) * 32);
-              const uint64_t a = tc::smem_desc_sw128(ka + goff, 16, 1024);
-              const uint64_t bd = tc::smem_desc_sw128(
-                  q_tile + (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32), 16, 1024);
-              tc::mma_bf16(tS0 + 16u * sb, a, bd, kIdescQK, kk > 0);
+              const uint32_t aoff = (uint32_t)((kk >> 2) * 2048 + (kk & 3) * 32);
+              const uint32_t boff = (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32);
+              tc::mma_bf16(tS0 + 16u * sb, a0 + (aoff >> 4), b0 + (boff >> 4), kIdescQK, kk > 0);
             }
             tc::mma_commit(bars.s_full + 8u * sb);
             tc_trace(p, 1, ntr, 3, (uint32_t)gk);
@@ -501,29 +562,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               ++qi;
               have_item = false;
             }
-            progress = true;
-          }
-        }
-        if (next_pv < next_qk) {
-          const int gk = next_pv;
-          const int slot = gk % NS;
-          const int sb = gk & 1;
-          if (mbar_test(bars.p_full + 8u * sb, (gk >> 1) & 1) &&
-              (gk < 2 || mbar_test(bars.o_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
-            tc::fence_after_sync();
-            const uint32_t va = sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)kRegion;
-            const uint32_t pt = p_s + (uint32_t)sb * 2u * kTcHeads * 128u;
-#pragma unroll
-            for (int kk = 0; kk < kPvSteps; ++kk) {
-              const uint64_t a = tc::smem_desc_sw128(va + (uint32_t)kk * 2048u, kPvLbo, 1024);
-              const uint64_t bd = tc::smem_desc_sw128(
-                  pt + (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32), 16, 1024);
-              tc::mma_bf16(tO0 + 16u * sb, a, bd, kIdescPV, kk > 0);
-            }
-            tc::mma_commit(bars.o_full + 8u * sb);
-            tc::mma_commit(bars.empty0 + 8u * slot);
-            tc_trace(p, 1, ntr, 4, (uint32_t)gk);
-            ++next_pv;
             progress = true;
           }
         }
@@ -584,7 +622,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       it.kind = ring[j].kind;
       ok = softmax_group_all(w && ok && !flags[0]);  // every thread has read the entry
       if (!ok) break;
-      if (tid == 64) mbar_arrive(bars.it_free + 8u * j);
+      if (tid == 64) {
+        mbar_arrive(bars.it_free + 8u * j);
+        tc_trace(p, 2, ntr, 14, (uint32_t)ii);
+      }
       if (it.kind == kItemEnd) break;
       const size_t row0 = (size_t)it.s * p.num_heads + (size_t)it.h * G;
       if (it.kind == kItemZero) {
@@ -608,6 +649,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int sb = g_k & 1;
         const int slot = g_k % NS;
         const bool ws = mbar_wait_bounded(bars.s_full + 8u * sb, (g_k >> 1) & 1, p.err);
+        if (tid == 64) tc_trace(p, 2, ntr, 15, (uint32_t)g_k);
         __syncwarp();
         tc::fence_after_sync();
         float sc[GP];
@@ -622,13 +664,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!valid) {
           // A stale row of V (past the sequence, or never loaded) must not
           // reach the PV product: 0 * NaN would.
-          const uint32_t vrow = sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)kRegion +
-                                (uint32_t)row * 128u;
+          const uint32_t vrow = sbase + (uint32_t)slot * (uint32_t)lay.stage +
+                                (uint32_t)((row >> 3) * kChunkBytes + 1024 + (row & 7) * 128);
 #pragma unroll
           for (int g = 0; g < kGroups; ++g)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              st_shared_zero16(vrow + (uint32_t)(g * kGroupBytes + c * 16));
+              st_shared_zero16(vrow + (uint32_t)(g * 2048 + c * 16));
         }
         float x[GP];
 #pragma unroll
@@ -672,7 +714,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_proxy_async_smem();
         mbar_arrive(bars.p_full + 8u * sb);
         if (tid == 64) tc_trace(p, 2, ntr, 6, (uint32_t)g_k);
-        if (k >= 1) ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, o_acc, alpha_prev) && ok;
+        else if (lane == 0) tc_trace(p, warp, ntr, 19, (uint32_t)((warp << 16) | g_k));
+        if (k >= 1) {
+          ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, o_acc, alpha_prev) && ok;
+          if (tid == 64) tc_trace(p, 2, ntr, 16, (uint32_t)(g_k - 1));
+        }
 #pragma unroll
         for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
       }
@@ -681,6 +727,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // warp executes the tensor-memory load convergently or not at all.
       if (!(ok = softmax_group_all(ok && !flags[0]))) break;
       ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, o_acc, alpha_prev);
+      if (tid == 64) tc_trace(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
       gk += n;
 
       // l over the warpgroup's 128 token rows, then the item's output.

@@ -25,6 +25,24 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel of the library is launched so that it may start while the
+// previous kernel on its stream is still finishing.  Before its first access
+// to global memory each thread waits until the grids it depends on have
+// completed and their writes are visible (a no-op for a kernel launched
+// without the attribute).  Every thread executes the wait, so no grid of the
+// library completes before the grid it follows: completion stays ordered
+// along the stream.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next grid on the stream start launching (its own wait still holds
+// it back until this grid has completed).
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier -------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -10,6 +10,24 @@ namespace pa {
 
 struct DecodeParams;
 
+// Launch `kernel` with programmatic stream serialization: it may begin (and
+// run the part before its grid_dependency_wait) while the previous kernel on
+// the stream finishes.  `args` points at the kernel's arguments, in order.
+inline cudaError_t launch_overlapped(const void* kernel, dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, void** args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
 cudaError_t launch_reshape_and_cache(void* cache, const void* key, const void* value,
                                      const int64_t* slot_mapping, int64_t num_tokens,
                                      int64_t num_slots, int row_bytes, int64_t plane_bytes,

@@ -70,6 +70,30 @@ def test_decode_argument_checks():
     assert call(hq=2 * 9, desc=desc(block_size=4)) == pa.PA_ERR_UNSUPPORTED     # 4-token blocks
 
 
+def test_kernel_selection_rule():
+    sel = pa.pa_decode_select_kernel
+    qwen = desc(block_size=16, num_kv_heads=2, head_size=64)
+    assert sel(qwen, 64, 14) == pa.PA_KERNEL_TENSOR                  # G = 7
+    opt = desc(block_size=16, num_kv_heads=40, head_size=128)
+    assert sel(opt, 32, 40) == pa.PA_KERNEL_SIMT                     # G = 1
+    assert sel(opt, 32, 40, kernel=pa.PA_KERNEL_TENSOR) == pa.PA_KERNEL_TENSOR
+    assert sel(qwen, 64, 14, kernel=pa.PA_KERNEL_SIMT) == pa.PA_KERNEL_SIMT
+    assert sel(qwen, 64, 14, query_ptr=256 + 8) == pa.PA_KERNEL_SIMT  # query not 16-byte aligned
+    assert sel(desc(block_size=4, num_kv_heads=2, head_size=64), 4, 8) == pa.PA_KERNEL_SIMT
+    f32 = desc(block_size=16, num_kv_heads=2, head_size=64, dtype=pa.PA_FP32)
+    assert sel(f32, 4, 8) == pa.PA_KERNEL_SIMT
+    with pytest.raises(pa.PAError) as e:
+        sel(f32, 4, 8, kernel=pa.PA_KERNEL_TENSOR)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+    assert sel(qwen, 4, 2 * 12) == pa.PA_KERNEL_TENSOR               # G = 12: tensor cores only
+    with pytest.raises(pa.PAError) as e:
+        sel(qwen, 4, 2 * 12, kernel=pa.PA_KERNEL_SIMT)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+    with pytest.raises(pa.PAError) as e:
+        sel(qwen, 4, 15)                                             # 15 % 2 != 0
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
 def test_partition_and_workspace_sizes():
     d = desc(block_size=16, num_kv_heads=8, head_size=128)
     assert pa.pa_decode_partition_size(d, 8, 32, 32768, 512) == 512

@@ -157,8 +157,8 @@ def test_decode_on_side_stream():
 def test_decode_trace_records_the_pipeline():
     case = workloads.custom(3, 8, 2, 64, 16, [300, 40, 700], "bf16", seed=21)
     dc = DeviceCase(case)
-    per_role = 256
-    buf = torch.zeros(304 * 3 * per_role * 2, dtype=torch.int64, device="cuda")
+    per_role, warps = 256, 6
+    buf = torch.zeros(304 * warps * per_role * 2, dtype=torch.int64, device="cuda")
     pa.pa_set_decode_trace(buf, per_role)
     try:
         out = dc.step(128, kernel=pa.PA_KERNEL_TENSOR)
@@ -167,16 +167,19 @@ def test_decode_trace_records_the_pipeline():
         pa.pa_set_decode_trace(None)
     ref, _ = oracle_reference(case)
     assert_close(to_f64(out), ref, "bf16")
-    ev = buf.view(-1, 3, per_role, 2).cpu().numpy()
+    ev = buf.view(-1, warps, per_role, 2).cpu().numpy()
     tags = (ev[..., 1] >> 32) & 0xFFFFFFFF
     starts = int((tags[:, 0, :] == 9).sum())
     assert starts >= 1
     items = 2 * sum(-(-int(n) // 128) for n in case.seq_lens)    # (seq, kv head, 128-token partition)
     stages = 2 * sum(-(-int(n) // 128) for n in case.seq_lens)   # one 128-token stage per partition
-    assert int((tags[:, 2, :] == 7).sum()) == items
-    assert int((tags[:, 0, :] == 2).sum()) == stages
-    assert int((tags[:, 1, :] == 3).sum()) == stages and int((tags[:, 1, :] == 4).sum()) == stages
+    count = lambda w, tag: int((tags[:, w, :] == tag).sum())
+    assert count(2, 7) == items
+    assert count(0, 2) == stages and count(0, 20) == stages
+    assert count(1, 3) == stages and count(1, 4) == stages and count(1, 17) == stages
+    assert count(2, 6) == stages
+    assert all(count(w, 19) == stages for w in (3, 4, 5))
     for cta in range(ev.shape[0]):
-        for role in range(3):
-            t = ev[cta, role, :, 0][tags[cta, role] != 0]
+        for w in range(warps):
+            t = ev[cta, w, :, 0][tags[cta, w] != 0]
             assert np.all(np.diff(t) >= 0)
