@@ -61,16 +61,31 @@ def make_workload(name: str):
     raise SystemExit("unknown workload %s" % name)
 
 
-def step_bytes(case) -> dict:
-    """Algorithmic bytes of one step: what the operations must read and write once."""
+# Workloads whose statement fixes the split-KV partition (512-token partitions
+# for the long-context batches); the others take the library's choice.
+WORKLOAD_PARTITION = {"long_context": 512, "long_context_mixed": 512}
+
+
+def step_bytes(case, partition: int = 0) -> dict:
+    """Algorithmic bytes of one step: what the operations must read and write
+    once.  With split-KV partitions, each sequence of more than one partition
+    also writes and reads its fp32 partials (head_size values and a log-sum-exp
+    per query head and partition)."""
     eb = workloads.elem_bytes(case.dtype)
     s, hq, hkv, d = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_size
     lens = case.seq_lens.astype(np.int64)
     blocks = int(((lens + case.block_size - 1) // case.block_size).sum())
     decode = case.kv_bytes() + 2 * s * hq * d * eb + 4 * blocks + 4 * s
+    partials = 0
+    if partition > 0:
+        parts = (lens + partition - 1) // partition
+        partials = int(parts[parts > 1].sum()) * hq * (d + 1) * 4 * 2
     t = int((lens > 0).sum())  # one new token per sequence
     write = t * hkv * d * eb * 2 * 2 + 8 * t  # read new K/V, write them, read slots
-    return {"decode": int(decode), "write": int(write), "step": int(decode + write)}
+    # "step": the workload's bytes, the same whatever partitions a run uses;
+    # "decode": what the decode call moves, partials included.
+    return {"decode": int(decode + partials), "partials": partials, "write": int(write),
+            "step": int(decode + write)}
 
 
 def measured_hbm_peak():
@@ -87,7 +102,7 @@ def kernel_source_digest() -> str:
     csrc = os.path.join(ROOT, "paged_kv_cache_78_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("decode") or f in ("pa_device.cuh",):
+        if f.startswith("decode") or f in ("pa_device.cuh", "pa_tcgen05.cuh", "api.cu"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode())
                 h.update(fh.read())
@@ -234,8 +249,9 @@ def run_gpu(args, rank, world, device):
 
     torch.cuda.set_device(device)
     case = make_workload(args.workload)
-    st = GpuStep(torch, pa, case, device, args.partition, args.kernel)
-    nbytes = step_bytes(case)
+    partition = args.partition if args.partition != -1 else WORKLOAD_PARTITION.get(args.workload, -1)
+    st = GpuStep(torch, pa, case, device, partition, args.kernel)
+    nbytes = step_bytes(case, st.partition)
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -447,7 +463,7 @@ def time_oracle(case, budget_s: float, steps: int = 0):
     return times, step, step.oracle.num_threads()
 
 
-def config_for(case, name):
+def config_for(case, name, partition=0):
     lens = case.seq_lens
     return {"workload": name, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
             "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
@@ -455,7 +471,7 @@ def config_for(case, name):
             "seq_len_min": int(lens.min()), "seq_len_max": int(lens.max()),
             "seq_len_mean": round(float(lens.mean()), 1),
             "new_tokens_per_step": int((lens > 0).sum()),
-            "bytes_per_step": step_bytes(case)["step"],
+            "bytes_per_step": step_bytes(case, partition)["step"],
             "l2": "flushed before every timed step (256 MB write, then 256 MB read)"}
 
 
@@ -555,7 +571,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if case.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": config_for(case, args.workload),
+        "config": config_for(case, args.workload, st.partition),
         "run": {"partition_size": st.partition, "cuda_graph": bool(args.graph),
                 "decode_kernel": {0: "auto", 1: "cuda cores", 2: "tensor cores"}[args.kernel] +
                                  " -> " + st.kernel_name,

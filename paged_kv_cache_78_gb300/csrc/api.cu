@@ -100,15 +100,36 @@ bool head_size_supported(int d) { return d == 64 || d == 128 || d == 256; }
 // 512, 256, 128, 64 tokens (not below the block size) that still gives about
 // three CTAs per SM when sequences average half of max_seq_len.  A size that
 // covers max_seq_len means no split (0).
-pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int max_seq_len,
+pa_status select_kernel(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_heads,
+                        const void* query, int32_t kernel, int32_t* selected);
+
+// The automatic partition size depends only on the shapes and on the kernel
+// family PA_KERNEL_AUTO picks for a 16-byte aligned query, so the size
+// queries and the decode call always agree.
+pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int num_heads, int max_seq_len,
                             int requested, int num_sms, int* out) {
   int p = requested;
   if (p == -1) {
-    p = 512;
     const long long heads = (long long)num_seqs * d->num_kv_heads;
-    while (p > 64 && p > d->block_size &&
-           heads * ((max_seq_len + p - 1) / p) < 6LL * num_sms)
-      p >>= 1;
+    int32_t family = PA_KERNEL_SIMT;
+    if (select_kernel(d, num_seqs, num_heads, reinterpret_cast<const void*>(256), PA_KERNEL_AUTO,
+                      &family) != PA_OK)
+      family = PA_KERNEL_SIMT;
+    if (family == PA_KERNEL_TENSOR) {
+      // Persistent tensor-core kernel: each work item pays a fixed cost to
+      // start and finish, so items are long (1024 tokens) unless that leaves
+      // fewer items than half the resident CTAs (two per SM for head size 64,
+      // one for 128).
+      const long long ctas = (long long)num_sms * (d->head_size == 64 ? 2 : 1);
+      p = 1024;
+      while (p > 128 && p > d->block_size && 2 * heads * ((max_seq_len + p - 1) / p) < ctas)
+        p >>= 1;
+    } else {
+      // One CTA per (partition, KV head, sequence): enough CTAs for six per SM.
+      p = 512;
+      while (p > 64 && p > d->block_size && heads * ((max_seq_len + p - 1) / p) < 6LL * num_sms)
+        p >>= 1;
+    }
     if (p < d->block_size) p = d->block_size;
   } else if (p < -1) {
     return PA_ERR_INVALID_ARG;
@@ -253,11 +274,14 @@ pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t partition_size, int32_t* resolved) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
-  if (!resolved || num_seqs < 0 || max_seq_len < 0 || num_heads < 1) return PA_ERR_INVALID_ARG;
+  if (!resolved || num_seqs < 0 || max_seq_len < 0 || num_heads < 1 ||
+      num_heads % desc->num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
   int sms = 0;
   if (partition_size == -1 && (st = device_state(nullptr, &sms)) != PA_OK) return st;
   int p = 0;
-  if ((st = resolve_partition(desc, num_seqs, max_seq_len, partition_size, sms, &p)) != PA_OK)
+  if ((st = resolve_partition(desc, num_seqs, num_heads, max_seq_len, partition_size, sms, &p)) !=
+      PA_OK)
     return st;
   *resolved = p;
   return PA_OK;
@@ -327,7 +351,8 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   int sms = 0;
   if ((st = device_state(&err, &sms)) != PA_OK) return st;
   int part = 0;
-  if ((st = resolve_partition(desc, num_seqs, max_seq_len, partition_size, sms, &part)) != PA_OK)
+  if ((st = resolve_partition(desc, num_seqs, num_heads, max_seq_len, partition_size, sms,
+                              &part)) != PA_OK)
     return st;
   const int max_parts = part > 0 ? (max_seq_len + part - 1) / part : 1;
   float* part_o = nullptr;
