@@ -242,6 +242,17 @@ class GpuStep:
                           self.partition, self.ws, kernel=self.kernel)
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks of the default
+    process group (each replica's time; the job takes as long as its slowest
+    rank)."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_gpu(args, rank, world, device):
     import torch
 
@@ -340,6 +351,8 @@ def run_gpu(args, rank, world, device):
         torch.distributed.barrier()
     step_ms = sum(a.elapsed_time(b) for a, b in ev)
     decode_ms = sum(a.elapsed_time(b) for a, b in ev_dec)
+    if world > 1:
+        step_ms, decode_ms = max_over_ranks([step_ms, decode_ms], device)
     flags = pa.pa_get_device_error()
     if flags:
         raise RuntimeError("device error word 0x%x after the timed region" % flags)
@@ -395,9 +408,7 @@ def run_gpu(args, rank, world, device):
         sampler.stop()
 
     if world > 1:
-        t = torch.tensor([step_ms, decode_ms, e2e_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, decode_ms, e2e_ms = t.tolist()
+        e2e_ms = max_over_ranks([e2e_ms], device)[0]
     return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
             "decode_ms": decode_ms / args.steps, "e2e_ms": e2e_ms, "clocks": clocks,
             "h2d": h2d, "d2h": d2h}
