@@ -387,6 +387,10 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
     prm.trace_bytes = g_trace_bytes.load();
     prm.total_items = (int)std::min<long long>((long long)num_seqs * desc->num_kv_heads * max_parts,
                                                (1ll << 31) - 1);
+    // With many partitions per sequence most (partition, sequence, head)
+    // slots of a mixed-length batch are past a sequence's end; the kernel
+    // then numbers only the real items (batches it caches in shared memory).
+    prm.dense_items = max_parts > 4 && num_seqs <= pa::kTcLensCache;
   } else {
     // 32-token stages, TMA boxes of min(block_size, 32) rows, one box per
     // 128-byte column group, each box at a 1024-byte aligned slot so the
@@ -411,8 +415,18 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
     if (ns >= pa::kConsumerWarps) ns -= ns % pa::kConsumerWarps;
     prm.num_stages = ns;
     prm.num_consumers = ns < pa::kConsumerWarps ? ns : pa::kConsumerWarps;
-    prm.group_slot = gslot;
-    prm.region_bytes = region;
+    prm.kv_boxes = R >= 8;
+    if (prm.kv_boxes) {
+      // One box per block: [column group][K or V][R rows of 128 bytes].
+      prm.group_slot = 2 * R * 128;
+      prm.region_bytes = R * 128;
+      prm.box_stride = groups * 2 * R * 128;
+    } else {
+      prm.group_slot = gslot;
+      prm.region_bytes = region;
+      prm.box_stride = groups * gslot;
+    }
+    prm.stage_bytes = stage_bytes;
     prm.stage_area = area_for(ns);
     smem = pa::decode_smem_bytes(prm.stage_area, group, D);
   }
@@ -449,6 +463,25 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
     const cuuint32_t tbox[5] = {64u, 8u, 2u, (cuuint32_t)(D / 64), (cuuint32_t)(R / 8)};
     cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), tdim,
                 tstride, tbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (prm.kv_boxes) {
+    // CUDA-core kernel, blocks of 8 tokens or more: one box per block holds
+    // its R rows of K and V for every column group, laid out
+    // [column group][K or V][rows].  Dimensions, innermost first: one
+    // 128-byte chunk; token within the block; K or V; (KV head, column
+    // group); block.
+    const cuuint64_t row = (cuuint64_t)desc->num_kv_heads * D * es;
+    const cuuint64_t kdim[5] = {(cuuint64_t)inner, (cuuint64_t)BS, 2ull,
+                                (cuuint64_t)desc->num_kv_heads * groups,
+                                (cuuint64_t)desc->num_blocks};
+    const cuuint64_t kstride[4] = {row, (cuuint64_t)desc->num_blocks * BS * row, 128ull,
+                                   (cuuint64_t)BS * row};
+    const cuuint32_t kbox[5] = {(cuuint32_t)inner, (cuuint32_t)R, 2u, (cuuint32_t)groups, 1u};
+    cr = encode(&map,
+                desc->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                5, const_cast<void*>(cache), kdim, kstride, kbox, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     cr = encode(&map,

@@ -11,9 +11,12 @@
 //
 // Work decomposition (one CTA = one (partition, KV head, sequence)):
 //   warp 0      producer: walks the partition's block table (32 entries per
-//               lane-parallel load) and issues one TMA box per (block, 128-byte
-//               column group, K or V) into a ring of shared-memory stages of
-//               32 tokens, completing on the stage's "full" mbarrier;
+//               lane-parallel load) and issues TMA boxes into a ring of
+//               shared-memory stages of 32 tokens, completing on the stage's
+//               "full" mbarrier: with blocks of 8 tokens or more one box per
+//               block holding its K and V rows of every 128-byte column group
+//               (laid out [column group][K or V][rows]), else one box per
+//               (block, column group, K or V);
 //   warps 1..4  consumers: warp w takes stages w, w+C, ... (C consumer warps,
 //               C dividing the number of stages, so that every ring slot has
 //               a single owner and each slot's barrier phases are waited on in
@@ -51,6 +54,7 @@ struct DecodeParams {
   unsigned int* err;            // device error word
   unsigned int* sched;          // tensor-core kernel: [0] next work item, [1] CTAs finished
   int total_items;              // tensor-core kernel: num_seqs * num_kv_heads * max_parts
+  int dense_items;              // tensor-core kernel: number only the real work items
   int num_seqs;
   unsigned long long* trace;    // tensor-core kernel timeline, or null
   int trace_per_role;
@@ -68,8 +72,11 @@ struct DecodeParams {
   // shared-memory geometry, bytes
   int box_rows;          // tokens per TMA box: min(block_size, tokens per stage)
   int log2_box_rows;
-  int group_slot;        // bytes per (box, 128-byte column group): max(box_rows*128, 1024)
-  int region_bytes;      // K (or V) part of one stage
+  int group_slot;        // bytes between a box's 128-byte column groups
+  int region_bytes;      // bytes from a K row to the same V row
+  int box_stride;        // bytes between consecutive boxes of a stage
+  int kv_boxes;          // 1: one TMA box per block holds K and V of every column group
+  int stage_bytes;       // bytes of one stage
   int num_stages;        // a multiple of num_consumers
   int num_consumers;     // consumer warps that take stages (1..kConsumerWarps)
   int stage_area;        // bytes before the query buffer (stages, or the merge overlay)
@@ -203,7 +210,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     int win = tok0 >> l2bs;                      // logical block held by lane 0 of `cur`
     int cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
     int nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
-    const uint32_t box_bytes = (uint32_t)R * 128u;
+    const uint32_t box_bytes = p.kv_boxes ? (uint32_t)R * (uint32_t)kGroups * 256u : (uint32_t)R * 128u;
+    const uint32_t stage_tx = p.kv_boxes ? box_bytes : (uint32_t)(kGroups * 2) * box_bytes;
     int issued = 0;
     for (int k = 0; k < n_stages; ++k) {
       const int slot = k % NS;
@@ -219,10 +227,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       const int st_tok = tok0 + k * kStageTokens;
       const int st_n = min(kStageTokens, tok1 - st_tok);
       const int nbox = (st_n + R - 1) >> log2R;
-      if (lane == 0)
-        mbar_arrive_expect_tx(full0 + 8u * slot, (uint32_t)(nbox * kGroups * 2) * box_bytes);
-      const uint32_t kdst = sbase + (uint32_t)slot * 2u * region;
-      for (int i = 0; i < nbox; ++i) {
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8u * slot, (uint32_t)nbox * stage_tx);
+      __syncwarp();
+      const uint32_t kdst = sbase + (uint32_t)slot * (uint32_t)p.stage_bytes;
+      if (p.kv_boxes) {
+        // One box per block, issued by one lane each (a stage holds at most
+        // 32 / 8 = 4 boxes, all inside the table window).
+        const int tk = st_tok + (min(lane, nbox - 1) << log2R);
+        const int lb = tk >> l2bs;
+        while ((st_tok >> l2bs) >= win + 32) {
+          cur = nxt;
+          win += 32;
+          nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+        }
+        const int src = lb - win;  // 0 .. 34
+        const int id_cur = __shfl_sync(0xffffffffu, cur, src & 31);
+        const int id_nxt = __shfl_sync(0xffffffffu, nxt, src & 31);
+        if (lane < nbox) {
+          int id = src < 32 ? id_cur : id_nxt;
+          if (id < 0 || id >= p.num_blocks) {
+            record_error(p.err, PA_DEVERR_BLOCK_ID);
+            id = p.num_blocks;  // outside the tensor: zero fill
+          }
+          tma_load_5d(kdst + (uint32_t)lane * (uint32_t)p.box_stride, &kv_map, full0 + 8u * slot,
+                      0, tk & (BS - 1), 0, h * kGroups, id);
+        }
+      }
+      for (int i = 0; !p.kv_boxes && i < nbox; ++i) {
         const int tk = st_tok + (i << log2R);
         const int lb = tk >> l2bs;
         const int t0 = tk & (BS - 1);
@@ -241,7 +272,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
           }
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
-            const uint32_t dst = kdst + (uint32_t)(i * kGroups + g) * gslot;
+            const uint32_t dst = kdst + (uint32_t)i * (uint32_t)p.box_stride + (uint32_t)g * gslot;
             tma_load_5d(dst, &kv_map, full0 + 8u * slot, 0, g, h, t0, ck);
             tma_load_5d(dst + region, &kv_map, full0 + 8u * slot, 0, g, h, t0, cv);
           }
@@ -261,7 +292,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     // This lane's token in the QK phase and its row position inside a stage.
     const int qk_box = lane >> log2R;
     const int qk_t = lane & (R - 1);
-    const uint32_t qk_off = (uint32_t)(qk_box * kGroups) * gslot + (uint32_t)qk_t * 128u;
+    const uint32_t qk_off = (uint32_t)qk_box * (uint32_t)p.box_stride + (uint32_t)qk_t * 128u;
     const uint32_t qk_swz = (uint32_t)(qk_t & 7);
 
     const int nc = p.num_consumers;
@@ -276,7 +307,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       }
       const int st_tok = tok0 + k * kStageTokens;
       const int nvalid = min(kStageTokens, tok1 - st_tok);
-      const uint32_t kreg = sbase + (uint32_t)slot * 2u * region;
+      const uint32_t kreg = sbase + (uint32_t)slot * (uint32_t)p.stage_bytes;
       const uint32_t vreg = kreg + region;
 
       // ---- scores: lane = token ----
@@ -332,7 +363,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       for (int j = pv_r; j < nvalid; j += kRpv) {
         const int box = j >> log2R;
         const int t = j & (R - 1);
-        const uint32_t rowbase = vreg + (uint32_t)(box * kGroups) * gslot + (uint32_t)t * 128u;
+        const uint32_t rowbase = vreg + (uint32_t)box * (uint32_t)p.box_stride + (uint32_t)t * 128u;
         float pw[kPStride];
         {
           const float4 a = lds128f(p_w_s + (uint32_t)(j * kPStride * 4));

@@ -46,7 +46,7 @@ constexpr int kTcHeads = 16;     // N of both MMAs: query heads, G padded
 constexpr int kTcThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr int kTcTmemCols = 64;  // S x2, O x2, 16 columns each
 constexpr int kTcItemRing = 4;
-constexpr int kTcLensCache = 512;  // batches up to this size keep seq_lens in shared memory
+constexpr int kTcLensCache = 256;  // batches up to this size keep seq_lens in shared memory
 constexpr int kTcTraceRoles = 6;   // timeline regions per CTA: one per warp
 
 // Kinds of ring entries.
@@ -69,6 +69,7 @@ struct TcSmem {
   int bar_off;
   int misc_off;
   int lens_off;  // cached sequence lengths (batches of up to kTcLensCache)
+  int pre_off;   // work items before each sequence (dense numbering), kTcLensCache + 1
   int total;     // bytes to request (includes 1024 of alignment slack)
 };
 
@@ -86,7 +87,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages) 
   // full/free [ring], drain
   l.misc_off = l.bar_off + 8 * (2 * num_stages + 14 + 2 * kTcItemRing + 1);
   l.lens_off = l.misc_off + 64;
-  l.total = l.lens_off + kTcLensCache * 4 + 1024;
+  l.pre_off = l.lens_off + kTcLensCache * 4;
+  l.total = l.pre_off + (kTcLensCache + 4) * 4 + 1024;
   return l;
 }
 
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // counter); the producer loads its block-table window now, overlapping the
   // sequence-length loads below.
   int pf_win = -1, pf_s = -1, pf_cur = 0, pf_nxt = 0;
-  if (warp == 0 && (int)blockIdx.x < p.total_items) {
+  if (warp == 0 && !p.dense_items && (int)blockIdx.x < p.total_items) {
     const int sh = p.num_seqs * p.num_kv_heads;
     const int part = (int)blockIdx.x / sh;
     pf_s = ((int)blockIdx.x - part * sh) / p.num_kv_heads;
@@ -302,13 +304,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int P = p.partition_tokens;
     int gk = 0, qi = 0, ii = 0, ntr = 0;
     if (lane == 0) tc_trace(p, 0, ntr, 9, p.trace ? (uint32_t)global_timer() : 0u);
+    // Dense numbering (many partitions per sequence, batches of up to
+    // kTcLensCache): sequence s owns items pre[s] .. pre[s+1]-1, its
+    // partitions in order with the KV heads fastest, so no index is spent on
+    // a partition past a sequence's end.  pre[] is a warp scan of the
+    // per-sequence item counts.  Otherwise item = (partition, sequence, KV
+    // head) over the whole grid, partitions past a sequence's end skipped.
+    int* pre = reinterpret_cast<int*>(base + lay.pre_off);
+    unsigned int total = (unsigned)p.total_items;
+    const bool dense = p.dense_items && lens_s != nullptr;
+    if (dense) {
+      int carry = 0;
+      if (lane == 0) pre[0] = 0;
+      for (int c0 = 0; c0 < p.num_seqs; c0 += 32) {
+        const int sq = c0 + lane;
+        int n = 0;
+        if (sq < p.num_seqs) {
+          const int L = lens_s[sq];
+          const int np = L <= 0 ? 1 : (P > 0 ? (L + P - 1) / P : 1);
+          if (L > 0 && ((P > 0 && np > p.max_parts) ||
+                        ((L + BS - 1) >> l2bs) > p.max_blocks_per_seq)) {
+            if (blockIdx.x == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
+          } else {
+            n = np * p.num_kv_heads;
+          }
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, n, o);
+          if (lane >= o) n += v;
+        }
+        if (sq < p.num_seqs) pre[sq + 1] = carry + n;
+        carry += __shfl_sync(0xffffffffu, n, 31);
+      }
+      __syncwarp();
+      total = (unsigned)carry;
+    }
     unsigned int idx = blockIdx.x;
     while (true) {
       if (flags[0]) break;
       // Lane 0 classifies the item; the warp follows its decision.
       TcItem it{0, 0, 0, 0, 0, 0, 0, kItemEnd};
       bool skip = false;
-      if (lane == 0 && idx < (unsigned)p.total_items) {
+      if (lane == 0 && dense && idx < total) {
+        // The sequence whose items contain idx: the last s with pre[s] <= idx.
+        int lo = 0, hi = p.num_seqs - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pre[mid] <= (int)idx) lo = mid; else hi = mid - 1;
+        }
+        const int r = (int)idx - pre[lo];
+        it.s = lo;
+        it.part = r / p.num_kv_heads;
+        it.h = r - it.part * p.num_kv_heads;
+        const int L = lens_s[lo];
+        if (L <= 0) {
+          it.kind = kItemZero;
+        } else {
+          const int nparts = P > 0 ? (L + P - 1) / P : 1;
+          it.kind = kItemAttend;
+          it.tok0 = P > 0 ? it.part * P : 0;
+          it.tok1 = P > 0 ? min(L, it.tok0 + P) : L;
+          it.nstages = (it.tok1 - it.tok0 + kTcTokens - 1) / kTcTokens;
+          it.final_out = nparts == 1;
+        }
+      } else if (lane == 0 && !dense && idx < total) {
         it.part = (int)(idx / (unsigned)sh);
         const int rem = (int)(idx % (unsigned)sh);
         it.s = rem / p.num_kv_heads;

@@ -74,6 +74,9 @@ SHAPES = [
     (24, 2, 128, 8, [8, 9, 300, 777], "bf16", (0, 256)),
     (16, 16, 128, 256, [100, 256, 700], "bf16", (0, 512)),
     (12, 1, 64, 32, [2, 4096], "bf16", (0, 640)),
+    # many partitions per sequence (the tensor-core kernel numbers only the
+    # real items), empty sequences first and last
+    (16, 4, 64, 16, [0, 1, 700, 3000, 129, 0], "bf16", (128, 512)),
 ]
 
 
