@@ -48,6 +48,7 @@ constexpr int kTcTmemCols = 64;  // S x2, O x2, 16 columns each
 constexpr int kTcItemRing = 4;
 constexpr int kTcLensCache = 256;  // batches up to this size keep seq_lens in shared memory
 constexpr int kTcTraceRoles = 6;   // timeline regions per CTA: one per warp
+constexpr float kTcLazyMax = 8.f;  // a stage's scores may exceed the running maximum by this much
 
 // Kinds of ring entries.
 constexpr int kItemAttend = 0;  // attention over tokens [tok0, tok1)
@@ -90,6 +91,37 @@ __host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages) 
   l.pre_off = l.lens_off + kTcLensCache * 4;
   l.total = l.pre_off + (kTcLensCache + 4) * 4 + 1024;
   return l;
+}
+
+// True in one lane of the (fully active) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
+// Has the phase with the given parity completed, as observed by every lane
+// of the warp?  (Each lane's own test gives it the acquire.)
+__device__ __forceinline__ bool warp_test(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_test(bar, parity));
+}
+
+// Named barrier of the softmax warpgroup that also ORs a predicate across it.
+__device__ __forceinline__ bool softmax_group_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
 }
 
 // Named barrier of the softmax warpgroup that also ANDs a predicate across it.
@@ -537,52 +569,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // issued as soon as their inputs are ready, independently, so a PV never
     // waits for an unrelated TMA load (PV releases the stage slot the loads
     // refill).  QK runs at most two stages ahead (S is double-buffered).
-    if (lane == 0) {
-      int next_qk = 0, next_pv = 0;  // global stage counters
-      int ii = 0, qi = 0, qb = 0, qk_k = 0, qk_n = 0;
-      bool have_item = false, need_q = false, end_seen = false, ok = true;
-      int ntr = 0;
-      long long t_idle = clock64();
-      while (true) {
-        bool progress = false;
-        if (!have_item && !end_seen) {
-          const int j = ii % kTcItemRing;
-          if (mbar_test(bars.it_full + 8u * j, (ii / kTcItemRing) & 1)) {
-            const int kind = ring[j].kind;
-            const int n = ring[j].nstages;
+    // The whole warp runs the loop with warp-uniform state (a barrier counts
+    // as complete once every lane has observed it, which also gives every
+    // lane its acquire), so the MMA operands are warp-uniform values; one
+    // elected lane issues the MMAs, commits and arrivals.
+    const bool leader = elect_one();
+    int next_qk = 0, next_pv = 0;  // global stage counters
+    int ii = 0, qi = 0, qb = 0, qk_k = 0, qk_n = 0;
+    bool have_item = false, need_q = false, end_seen = false, ok = true;
+    int ntr = 0;
+    long long t_idle = clock64();
+    while (true) {
+      bool progress = false;
+      if (!have_item && !end_seen) {
+        const int j = ii % kTcItemRing;
+        if (warp_test(bars.it_full + 8u * j, (ii / kTcItemRing) & 1)) {
+          const int kind = ring[j].kind;
+          const int n = ring[j].nstages;
+          __syncwarp();
+          if (leader) {
             mbar_arrive(bars.it_free + 8u * j);
             tc_trace(p, 1, ntr, 13, (uint32_t)ii);
-            ++ii;
-            progress = true;
-            if (kind == kItemEnd) {
-              end_seen = true;
-            } else if (kind == kItemAttend) {
-              have_item = true;
-              need_q = true;
-              qk_k = 0;
-              qk_n = n;
-              qb = qi & 1;
-            }
+          }
+          ++ii;
+          progress = true;
+          if (kind == kItemEnd) {
+            end_seen = true;
+          } else if (kind == kItemAttend) {
+            have_item = true;
+            need_q = true;
+            qk_k = 0;
+            qk_n = n;
+            qb = qi & 1;
           }
         }
-        if (have_item && need_q && mbar_test(bars.q_full + 8u * qb, (qi >> 1) & 1)) {
-          need_q = false;
-          progress = true;
-        }
-        if (next_pv < next_qk) {
-          const int gk = next_pv;
-          const int slot = gk % NS;
-          const int sb = gk & 1;
-          if (mbar_test(bars.p_full + 8u * sb, (gk >> 1) & 1) &&
-              (gk < 2 || mbar_test(bars.o_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+      }
+      if (have_item && need_q && warp_test(bars.q_full + 8u * qb, (qi >> 1) & 1)) {
+        need_q = false;
+        progress = true;
+      }
+      if (next_pv < next_qk) {
+        const int gk = next_pv;
+        const int slot = gk % NS;
+        const int sb = gk & 1;
+        if (warp_test(bars.p_full + 8u * sb, (gk >> 1) & 1) &&
+            (gk < 2 || warp_test(bars.o_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+          tc::fence_after_sync();
+          // A: the stage's V rows read MN-major (V^T), 64-dimension groups
+          // kPvLbo apart, 8-token groups kChunkBytes apart; B: P^T.
+          const uint64_t a0 = tc::smem_desc_sw128(
+              sbase + (uint32_t)slot * (uint32_t)lay.stage + 1024u, kPvLbo, kChunkBytes);
+          const uint64_t b0 = tc::smem_desc_sw128(p_s + (uint32_t)sb * 2u * kTcHeads * 128u, 16,
+                                                  1024);
+          if (leader) {
             tc_trace(p, 1, ntr, 17, (uint32_t)gk);
-            tc::fence_after_sync();
-            // A: the stage's V rows read MN-major (V^T), 64-dimension groups
-            // kPvLbo apart, 8-token groups kChunkBytes apart; B: P^T.
-            const uint64_t a0 = tc::smem_desc_sw128(
-                sbase + (uint32_t)slot * (uint32_t)lay.stage + 1024u, kPvLbo, kChunkBytes);
-            const uint64_t b0 = tc::smem_desc_sw128(p_s + (uint32_t)sb * 2u * kTcHeads * 128u, 16,
-                                                    1024);
 #pragma unroll
             for (int kk = 0; kk < kPvSteps; ++kk) {
               const uint32_t aoff = (uint32_t)(kk * 2 * kChunkBytes);
@@ -592,22 +632,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::mma_commit(bars.o_full + 8u * sb);
             tc::mma_commit(bars.empty0 + 8u * slot);
             tc_trace(p, 1, ntr, 4, (uint32_t)gk);
-            ++next_pv;
-            progress = true;
           }
+          __syncwarp();
+          ++next_pv;
+          progress = true;
         }
-        if (have_item && !need_q && next_qk < next_pv + 2) {
-          const int gk = next_qk;
-          const int slot = gk % NS;
-          const int sb = gk & 1;
-          if (mbar_test(bars.full0 + 8u * slot, (gk / NS) & 1) &&
-              (gk < 2 || mbar_test(bars.s_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
-            tc::fence_after_sync();
-            // A: the stage's K rows, K-major, 8-row groups kChunkBytes apart;
-            // B: the item's Q tile.  Descriptors advance by address / 16.
-            const uint64_t a0 = tc::smem_desc_sw128(sbase + (uint32_t)slot * (uint32_t)lay.stage,
-                                                    16, kChunkBytes);
-            const uint64_t b0 = tc::smem_desc_sw128(q_s + (uint32_t)(qb * kQTile), 16, 1024);
+      }
+      if (have_item && !need_q && next_qk < next_pv + 2) {
+        const int gk = next_qk;
+        const int slot = gk % NS;
+        const int sb = gk & 1;
+        if (warp_test(bars.full0 + 8u * slot, (gk / NS) & 1) &&
+            (gk < 2 || warp_test(bars.s_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+          tc::fence_after_sync();
+          // A: the stage's K rows, K-major, 8-row groups kChunkBytes apart;
+          // B: the item's Q tile.  Descriptors advance by address / 16.
+          const uint64_t a0 = tc::smem_desc_sw128(sbase + (uint32_t)slot * (uint32_t)lay.stage,
+                                                  16, kChunkBytes);
+          const uint64_t b0 = tc::smem_desc_sw128(q_s + (uint32_t)(qb * kQTile), 16, 1024);
+          const bool last = qk_k + 1 == qk_n;
+          if (leader) {
 #pragma unroll
             for (int kk = 0; kk < kKSteps; ++kk) {
               const uint32_t aoff = (uint32_t)((kk >> 2) * 2048 + (kk & 3) * 32);
@@ -615,46 +659,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc::mma_bf16(tS0 + 16u * sb, a0 + (aoff >> 4), b0 + (boff >> 4), kIdescQK, kk > 0);
             }
             tc::mma_commit(bars.s_full + 8u * sb);
+            if (last) tc::mma_commit(bars.q_free + 8u * qb);  // the item's Q tile is no longer read
             tc_trace(p, 1, ntr, 3, (uint32_t)gk);
-            ++next_qk;
-            if (++qk_k == qk_n) {
-              tc::mma_commit(bars.q_free + 8u * qb);  // the item's Q tile is no longer read
-              ++qi;
-              have_item = false;
-            }
-            progress = true;
           }
-        }
-        if (end_seen && !have_item && next_pv == next_qk) break;
-        if (progress) {
-          t_idle = clock64();
-        } else if (!flags[0]) {
-          // Nothing ready: suspend briefly (128 ns at most) on the barrier most
-          // likely to unblock this loop (the oldest pending PV's P tile, else
-          // the next QK's stage); it wakes early when that barrier completes,
-          // and leaves issue slots to the softmax warp sharing its scheduler.
-          if (next_pv < next_qk)
-            mbar_suspend(bars.p_full + 8u * (next_pv & 1), (next_pv >> 1) & 1, 128);
-          else if (have_item && !need_q)
-            mbar_suspend(bars.full0 + 8u * (next_qk % NS), (next_qk / NS) & 1, 128);
-          else if (have_item)
-            mbar_suspend(bars.q_full + 8u * qb, (qi >> 1) & 1, 128);
-          else if (!end_seen)
-            mbar_suspend(bars.it_full + 8u * (ii % kTcItemRing), (ii / kTcItemRing) & 1, 128);
-        }
-        if (progress) {
-        } else if (flags[0]) {
-          ok = false;
-          break;
-        } else if (clock64() - t_idle > kWaitLimitCycles) {
-          record_error(p.err, PA_DEVERR_TIMEOUT);
-          ok = false;
-          break;
+          __syncwarp();
+          ++next_qk;
+          if (++qk_k == qk_n) {
+            ++qi;
+            have_item = false;
+          }
+          progress = true;
         }
       }
-      if (!ok) flags[0] = 1;
-      // Every MMA this thread issued completes before the CTA may free its
-      // tensor memory.
+      if (end_seen && !have_item && next_pv == next_qk) break;
+      const bool abort = __any_sync(0xffffffffu, flags[0] != 0);
+      if (progress) {
+        t_idle = clock64();
+      } else if (!abort) {
+        // Nothing ready: suspend briefly (128 ns at most) on the barrier most
+        // likely to unblock this loop (the oldest pending PV's P tile, else
+        // the next QK's stage); it wakes early when that barrier completes,
+        // and leaves issue slots to the softmax warp sharing its scheduler.
+        if (next_pv < next_qk)
+          mbar_suspend(bars.p_full + 8u * (next_pv & 1), (next_pv >> 1) & 1, 128);
+        else if (have_item && !need_q)
+          mbar_suspend(bars.full0 + 8u * (next_qk % NS), (next_qk / NS) & 1, 128);
+        else if (have_item)
+          mbar_suspend(bars.q_full + 8u * qb, (qi >> 1) & 1, 128);
+        else if (!end_seen)
+          mbar_suspend(bars.it_full + 8u * (ii % kTcItemRing), (ii / kTcItemRing) & 1, 128);
+      }
+      if (progress) {
+      } else if (abort) {
+        ok = false;
+        break;
+      } else if (__any_sync(0xffffffffu, clock64() - t_idle > kWaitLimitCycles)) {
+        if (leader) record_error(p.err, PA_DEVERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+    }
+    if (!ok && leader) flags[0] = 1;
+    // Every MMA the leader issued completes before the CTA may free its
+    // tensor memory.
+    if (leader) {
       tc::mma_commit(bars.drain);
       mbar_wait_bounded(bars.drain, 0, p.err);
     }
@@ -736,27 +784,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int g = 0; g < GP; ++g)
           x[g] = (valid && g < G) ? sc[g] * p.scale_log2 : -INFINITY;
-        float* redk = red + sb * 4 * kTcHeads;
+        // Lazy reference maximum: m_run[g] only has to bound this stage's
+        // scores to within kTcLazyMax (log2 units), so the weights 2^(x - m)
+        // stay at most 2^kTcLazyMax, exact in bf16 and fp32 sums.  Only when
+        // some score in the warpgroup exceeds it (always on an item's first
+        // stage) is the maximum exchanged and the running sums rescaled;
+        // otherwise the stage costs one barrier.  A failed wait anywhere also
+        // takes the exchange path, whose AND-barrier makes every thread agree.
+        bool need = !(ws && ok) || flags[0];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          const float wm = warp_max(x[g]);
-          if (lane == 0) redk[q4 * kTcHeads + g] = wm;
-        }
-        if (!(ok = softmax_group_all(ws && ok && !flags[0]))) break;
+        for (int g = 0; g < GP; ++g) need |= x[g] > m_run[g] + kTcLazyMax;
         float alpha[GP], pr[GP];
 #pragma unroll
+        for (int g = 0; g < GP; ++g) alpha[g] = 1.f;
+        if (softmax_group_any(need)) {
+          float* redk = red + sb * 4 * kTcHeads;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            const float wm = warp_max(x[g]);
+            if (lane == 0) redk[q4 * kTcHeads + g] = wm;
+          }
+          if (!(ok = softmax_group_all(ws && ok && !flags[0]))) break;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            // Heads g >= G are padding: their scores are all -inf, the
+            // maximum stays -inf, and they are given weight 0 and factor 1.
+            const float tmax = fmaxf(fmaxf(redk[g], redk[kTcHeads + g]),
+                                     fmaxf(redk[2 * kTcHeads + g], redk[3 * kTcHeads + g]));
+            const float m_new = fmaxf(m_run[g], tmax);
+            if (g < G) alpha[g] = fast_exp2(m_run[g] - m_new);
+            m_run[g] = m_new;
+          }
+        }
+#pragma unroll
         for (int g = 0; g < GP; ++g) {
-          // Heads g >= G are padding: their scores are all -inf, the
-          // maximum stays -inf, and they are given weight 0 and factor 1.
-          const float tmax = fmaxf(fmaxf(redk[g], redk[kTcHeads + g]),
-                                   fmaxf(redk[2 * kTcHeads + g], redk[3 * kTcHeads + g]));
-          const float m_new = fmaxf(m_run[g], tmax);
-          const bool real = g < G;
-          alpha[g] = real ? fast_exp2(m_run[g] - m_new) : 1.f;
-          m_run[g] = m_new;
           // The weight enters P.V rounded to bf16; the denominator sums the
           // same rounded weights, so the output stays a convex combination.
-          pr[g] = real ? __bfloat162float(__float2bfloat16_rn(fast_exp2(x[g] - m_new))) : 0.f;
+          pr[g] = g < G ? __bfloat162float(__float2bfloat16_rn(fast_exp2(x[g] - m_run[g]))) : 0.f;
           l_run[g] = fmaf(l_run[g], alpha[g], pr[g]);
         }
         // P^T as the PV's B operand: [64-token group][16 rows][128 bytes], swizzled.
