@@ -53,8 +53,11 @@ cudaError_t launch_reduce_for_head_size(void* out, const float* part_o, const fl
                                         const int32_t* seq_lens, int num_seqs, int num_heads,
                                         int partition_tokens, int max_parts,
                                         cudaStream_t stream) {
-  dim3 grid((unsigned)num_heads, (unsigned)num_seqs);
-  void* args[] = {&out, &part_o, &part_lse, &seq_lens, &num_heads, &partition_tokens, &max_parts};
+  // Rows of many partitions are shared by several CTAs (32 columns each).
+  int cols = max_parts >= 128 ? kReduceMinCols : D;
+  dim3 grid((unsigned)num_heads, (unsigned)num_seqs, (unsigned)(D / cols));
+  void* args[] = {&out, &part_o, &part_lse, &seq_lens, &num_heads, &partition_tokens, &max_parts,
+                  &cols};
   return launch_overlapped((const void*)lse_reduce_kernel<T, D>, grid, dim3(kReduceThreads), 0,
                            stream, args);
 }

@@ -472,30 +472,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
 // Log-sum-exp combination of split-KV partials:
 //   M = max_p lse_p,  w_p = 2^(lse_p - M),  out = sum_p w_p o_p / sum_p w_p.
-// One CTA per (query head, sequence).  Its threads split the partitions into
-// kReduceThreads / (D / 4) slices, each thread summing float4 columns of its
-// slice's partials (four loads in flight); the slices are then added through
+// One CTA per (query head, sequence, `cols` output columns): cols = D, or 32
+// when rows have many partitions (more CTAs share a long row).  Its threads
+// are cols/4 float4 columns x (1024/cols) partition slices; each sums its
+// slice's partials (four loads in flight), and the slices are added through
 // shared memory.  The weights of up to kReduceChunk partitions at a time are
 // staged in shared memory.
 constexpr int kReduceThreads = 256;
 constexpr int kReduceChunk = 1024;
+constexpr int kReduceMinCols = 32;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads, 4)
     lse_reduce_kernel(void* out_, const float* __restrict__ part_o,
                       const float* __restrict__ part_lse, const int32_t* __restrict__ seq_lens,
-                      int num_heads, int partition_tokens, int max_parts) {
+                      int num_heads, int partition_tokens, int max_parts, int cols) {
   using E = ElemTraits<T>;
-  constexpr int kCols = D / 4;                      // float4 columns of a row
-  constexpr int kSlices = kReduceThreads / kCols;   // partitions summed in parallel
-  static_assert(kReduceThreads % kCols == 0 && kSlices >= 1, "reduce shape");
+  static_assert(D % kReduceMinCols == 0, "reduce columns");
+  constexpr int kRowF4 = D / 4;  // float4 columns of a partial row
   __shared__ float w_s[kReduceChunk];
-  __shared__ __align__(16) float acc_s[kSlices][D];
+  __shared__ __align__(16) float acc_s[kReduceThreads * 4];
   __shared__ float red_s[kReduceThreads / 32];
   __shared__ float bcast_s;
 
   const int hq = blockIdx.x;
   const int s = blockIdx.y;
+  const int col0 = blockIdx.z * cols;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
   if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
   const size_t row = (size_t)s * num_heads + hq;
   const float* lse = part_lse + row * max_parts;
-  const float4* po = reinterpret_cast<const float4*>(part_o + row * max_parts * D);
+  const float4* po = reinterpret_cast<const float4*>(part_o + row * max_parts * D + col0);
 
   // M over the row's partitions.
   float m = -INFINITY;
@@ -521,8 +523,10 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
   __syncthreads();
   const float M = bcast_s;
 
-  const int col = tid % kCols;
-  const int slice = tid / kCols;
+  const int ncol4 = cols >> 2;
+  const int col = tid % ncol4;
+  const int slice = tid / ncol4;
+  const int nslices = kReduceThreads / ncol4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   for (int c0 = 0; c0 < nparts; c0 += kReduceChunk) {
@@ -535,13 +539,13 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
     }
     __syncthreads();
     int q = slice;
-    for (; q + 3 * kSlices < cn; q += 4 * kSlices) {
-      const float4 a = po[(size_t)(c0 + q) * kCols + col];
-      const float4 b = po[(size_t)(c0 + q + kSlices) * kCols + col];
-      const float4 c = po[(size_t)(c0 + q + 2 * kSlices) * kCols + col];
-      const float4 d = po[(size_t)(c0 + q + 3 * kSlices) * kCols + col];
-      const float wa = w_s[q], wb = w_s[q + kSlices], wc = w_s[q + 2 * kSlices],
-                  wd = w_s[q + 3 * kSlices];
+    for (; q + 3 * nslices < cn; q += 4 * nslices) {
+      const float4 a = po[(size_t)(c0 + q) * kRowF4 + col];
+      const float4 b = po[(size_t)(c0 + q + nslices) * kRowF4 + col];
+      const float4 c = po[(size_t)(c0 + q + 2 * nslices) * kRowF4 + col];
+      const float4 d = po[(size_t)(c0 + q + 3 * nslices) * kRowF4 + col];
+      const float wa = w_s[q], wb = w_s[q + nslices], wc = w_s[q + 2 * nslices],
+                  wd = w_s[q + 3 * nslices];
       acc.x = fmaf(wa, a.x, acc.x); acc.y = fmaf(wa, a.y, acc.y);
       acc.z = fmaf(wa, a.z, acc.z); acc.w = fmaf(wa, a.w, acc.w);
       acc.x = fmaf(wb, b.x, acc.x); acc.y = fmaf(wb, b.y, acc.y);
@@ -551,23 +555,23 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
       acc.x = fmaf(wd, d.x, acc.x); acc.y = fmaf(wd, d.y, acc.y);
       acc.z = fmaf(wd, d.z, acc.z); acc.w = fmaf(wd, d.w, acc.w);
     }
-    for (; q < cn; q += kSlices) {
-      const float4 a = po[(size_t)(c0 + q) * kCols + col];
+    for (; q < cn; q += nslices) {
+      const float4 a = po[(size_t)(c0 + q) * kRowF4 + col];
       const float wa = w_s[q];
       acc.x = fmaf(wa, a.x, acc.x); acc.y = fmaf(wa, a.y, acc.y);
       acc.z = fmaf(wa, a.z, acc.z); acc.w = fmaf(wa, a.w, acc.w);
     }
   }
-  reinterpret_cast<float4*>(&acc_s[slice][0])[col] = acc;
+  reinterpret_cast<float4*>(acc_s)[tid] = acc;  // float index slice * cols + col * 4
   wsum = warp_sum(wsum);
   if (lane == 0) red_s[warp] = wsum;
   __syncthreads();
-  if (tid < D) {
+  if (tid < cols) {
     float ws = 0.f;
     for (int i = 0; i < kReduceThreads / 32; ++i) ws += red_s[i];
     float v = 0.f;
-    for (int i = 0; i < kSlices; ++i) v += acc_s[i][tid];
-    reinterpret_cast<T*>(out_)[row * D + tid] = E::from_float(v / ws);
+    for (int i = 0; i < nslices; ++i) v += acc_s[i * cols + tid];
+    reinterpret_cast<T*>(out_)[row * D + col0 + tid] = E::from_float(v / ws);
   }
 }
 
