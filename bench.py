@@ -353,6 +353,49 @@ def run_gpu(args, rank, world, device):
     decode_ms = sum(a.elapsed_time(b) for a, b in ev_dec)
     if world > 1:
         step_ms, decode_ms = max_over_ranks([step_ms, decode_ms], device)
+
+    # Outside the timed steps: the decode call warm (no eviction, inputs left
+    # in L2 by the previous call), and the same tokens in the unpaged layout
+    # (consecutive blocks), L2 evicted, to report what paging costs.
+    paging = None
+    if args.paging and world == 1:
+        n = max(50, args.steps // 4)
+        warm = [mk() for _ in range(n)]
+        for e0, e1 in warm:
+            e0.record(stream)
+            decode()
+            e1.record(stream)
+        st_c = GpuStep(torch, pa, workloads.contiguous(case), device, st.partition, args.kernel)
+        st_c.write()
+        st_c.decode()
+        g_c = None
+        if args.graph:
+            torch.cuda.synchronize()
+            g_c = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_c):
+                st_c.decode()
+        cont = [mk() for _ in range(n)]
+        for _ in range(3):
+            flush.zero_()
+            g_c.replay() if g_c else st_c.decode()
+        for e0, e1 in cont:
+            flush.zero_()
+            st_c.write()
+            e0.record(stream)
+            g_c.replay() if g_c else st_c.decode()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        warm_us = sum(a.elapsed_time(b) for a, b in warm) / n * 1e3
+        cont_us = sum(a.elapsed_time(b) for a, b in cont) / n * 1e3
+        paged_us = decode_ms / args.steps * 1e3
+        paging = {"paged_us_per_launch": round(paged_us, 2),
+                  "contiguous_us_per_launch": round(cont_us, 2),
+                  "overhead": round(paged_us / cont_us - 1.0, 4),
+                  "warm_us_per_launch": round(warm_us, 2),
+                  "launches": n,
+                  "note": "decode call on the same tokens with consecutive physical blocks "
+                          "(L2 evicted), and the paged call without eviction (warm)"}
+        del st_c, g_c
     flags = pa.pa_get_device_error()
     if flags:
         raise RuntimeError("device error word 0x%x after the timed region" % flags)
@@ -388,7 +431,7 @@ def run_gpu(args, rank, world, device):
             sampler.stop()
         return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
                 "decode_ms": decode_ms / args.steps, "e2e_ms": None, "clocks": clocks,
-                "h2d": h2d, "d2h": d2h}
+                "h2d": h2d, "d2h": d2h, "paging": paging}
     for _ in range(max(3, args.warmup // 4)):
         flush.zero_()
         e2e_step()
@@ -411,7 +454,7 @@ def run_gpu(args, rank, world, device):
         e2e_ms = max_over_ranks([e2e_ms], device)[0]
     return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
             "decode_ms": decode_ms / args.steps, "e2e_ms": e2e_ms, "clocks": clocks,
-            "h2d": h2d, "d2h": d2h}
+            "h2d": h2d, "d2h": d2h, "paging": paging}
 
 
 # ---------------------------------------------------------------------------
@@ -503,6 +546,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the CPU baseline (0 = skip)")
     ap.add_argument("--e2e", type=int, default=1, help="also time the step with host buffers")
+    ap.add_argument("--paging", type=int, default=1,
+                    help="also time the decode warm and on the unpaged (consecutive-block) layout")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
@@ -603,6 +648,7 @@ def main():
             "traffic": ncu_traffic(args.workload),
         },
         "e2e": e2e,
+        "paging": r["paging"],
         "clocks": r["clocks"],
         "cpu_baseline": cpu,
     }

@@ -228,6 +228,20 @@ def test_decode_block_relabelling_is_bit_identical():
     assert np.array_equal(got, ref)
 
 
+def test_unpaged_layout_of_the_same_tokens_gives_the_same_output():
+    # The bench's paging-overhead run: consecutive physical blocks are one more
+    # relabelling of the same tokens.
+    case = workloads.custom(4, 4, 2, 64, 8, [5, 40, 64, 77], "bf16", seed=9)
+    flat = workloads.contiguous(case)
+    assert [list(r[:-(-int(n) // 8)]) for r, n in zip(flat.block_tables, flat.seq_lens)] == \
+        [[0], [1, 2, 3, 4, 5], [6, 7, 8, 9, 10, 11, 12, 13], list(range(14, 24))]
+    ref = oracle.decode(case.query, oracle.fill_cache(case), case.block_tables, case.seq_lens,
+                        case.scale)
+    got = oracle.decode(flat.query, oracle.fill_cache(flat), flat.block_tables, flat.seq_lens,
+                        flat.scale)
+    assert np.array_equal(got, ref)
+
+
 def test_decode_single_token_returns_its_value():
     case = workloads.custom(3, 4, 4, 64, 4, [1, 1, 1], "bf16", seed=3)
     cache = oracle.fill_cache(case)

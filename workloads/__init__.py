@@ -156,6 +156,16 @@ def _tables_from_permutation(perm: np.ndarray, seq_lens: np.ndarray, block_size:
     return tables
 
 
+def contiguous(case: "DecodeCase") -> "DecodeCase":
+    """The same tokens with each sequence's logical blocks on consecutive
+    physical blocks (sequence after sequence from block 0): the unpaged
+    layout, for measuring what scattering the blocks costs."""
+    tables = _tables_from_permutation(np.arange(case.num_blocks, dtype=np.int32), case.seq_lens,
+                                      case.block_size, max_blocks=case.block_tables.shape[1])
+    return DecodeCase(**{**case.__dict__, "name": case.name + "_contiguous",
+                         "block_tables": tables})
+
+
 def _token_data(rng, seq_lens, hkv, d, dtype):
     starts = np.zeros(len(seq_lens) + 1, dtype=np.int64)
     starts[1:] = np.cumsum(seq_lens.astype(np.int64))
