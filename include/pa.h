@@ -294,6 +294,42 @@ pa_status pa_pool_ref_count(const pa_pool* pool, int32_t block, int32_t* ref);
 int32_t pa_pool_num_free(const pa_pool* pool);
 
 /* ---------------------------------------------------------------------------
+ * Prefix caching on the pool (itan.pw "vLLMにおけるKVCacheマネージャーの詳細
+ * 解説", sections "KVCacheManagerの処理詳細" and "プレイフィックスキャッシュの
+ * 詳細": requests that begin with the same tokens share the KV blocks of that
+ * prefix; only whole blocks are shared, and only a prefix that matches from
+ * the first token).
+ *   - A sequence created by pa_pool_add_seq_tokens knows its token ids.  Each
+ *     of its full blocks gets a chained hash (the previous block's hash and
+ *     the block's block_size token ids; 128 bits) and is registered under it
+ *     unless another block already is.  A partly filled block has no hash.
+ *   - pa_pool_add_seq_tokens shares the longest run of leading blocks whose
+ *     hashes are registered, at most (num_tokens - 1) / block_size of them
+ *     (the last prompt token is always computed); a shared block gains a
+ *     reference and, if it was free, leaves the free queue before the
+ *     request's other blocks are taken from the front of the queue.
+ *     *num_cached_tokens = shared blocks * block_size: the caller writes the
+ *     KV of tokens [*num_cached_tokens, num_tokens) (pa_reshape_and_cache)
+ *     before any sequence reads them.  Out of blocks: nothing changes.
+ *   - pa_pool_append_token_id appends like pa_pool_append_token and records
+ *     the token id; a block it fills is registered.  pa_pool_append_token(s)
+ *     on such a sequence drops it from prefix caching (no token id).
+ *   - A freed block keeps its hash (it can still be shared) until the free
+ *     queue hands it out for new content.  pa_pool_fork copies the token ids.
+ *   - pa_pool_is_cached: whether the block is registered.  pa_pool_free_queue:
+ *     the free queue front to back (cap entries into out; *n = its length).
+ *     pa_pool_reset_prefix_cache: forget every registration (blocks, counts
+ *     and tables unchanged).
+ * ------------------------------------------------------------------------- */
+pa_status pa_pool_add_seq_tokens(pa_pool* pool, const int32_t* tokens, int64_t num_tokens,
+                                 int64_t* seq_id, int64_t* num_cached_tokens);
+pa_status pa_pool_append_token_id(pa_pool* pool, int64_t seq, int32_t token, int64_t* slot,
+                                  int64_t cow_pair[2]);
+pa_status pa_pool_is_cached(const pa_pool* pool, int32_t block, int32_t* cached);
+pa_status pa_pool_free_queue(const pa_pool* pool, int32_t* out, int32_t cap, int32_t* n);
+pa_status pa_pool_reset_prefix_cache(pa_pool* pool);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics.
  * pa_get_device_error synchronises `stream`, returns the current device's
  * error word (PA_DEVERR_* bits) in *flags and clears it.  Returns

@@ -34,6 +34,21 @@ Rules, in the pages' terms:
   order), and appended at the tail of the FIFO free list (the front is where
   ``pop(0)`` takes new blocks in tech.blogsailing.com/?p=100).
 * Running out of free blocks is reported and leaves the state unchanged.
+
+Prefix caching (itan.pw page, sections "KVCacheManagerの処理詳細" and
+"プレイフィックスキャッシュの詳細"), written here with the exact token prefix as
+the key instead of a chained hash:
+
+* a full block of a sequence whose token ids are known is registered under
+  the tuple of all tokens up to its end (that is what the chained hash
+  identifies); a partly filled block is not;
+* a new request shares the longest run of leading registered blocks, at most
+  (num_tokens - 1) // block_size (the page's ``max_length = num_tokens - 1``
+  and ``max_num_blocks = max_length // block_size``), stopping at the first
+  miss; shared blocks leave the free queue before any block is taken for the
+  rest of the request (time 6 of the page's timeline);
+* freed blocks stay registered until the free queue hands them out again
+  (time 4: blocks 2 and 3 are free and still cached).
 """
 from __future__ import annotations
 
@@ -58,20 +73,63 @@ class PoolReplay:
         self.tables: dict[int, list[int]] = {}
         self.lens: dict[int, int] = {}
         self.next_id = 0
+        self.toks: dict[int, list[int] | None] = {}  # token ids of tracked sequences
+        self.cache: dict[tuple, int] = {}            # token prefix -> registered block
+        self.block_key: dict[int, tuple] = {}        # registered block -> its prefix
+
+    def _take(self) -> int:
+        b = self.free.popleft()
+        key = self.block_key.pop(b, None)
+        if key is not None:
+            del self.cache[key]
+        self.ref[b] = 1
+        return b
+
+    def _register(self, b: int, key: tuple) -> None:
+        if key not in self.cache and b not in self.block_key:
+            self.cache[key] = b
+            self.block_key[b] = key
 
     # -- operations -------------------------------------------------------
     def add_seq(self, num_tokens: int) -> int:
         need = -(-num_tokens // self.block_size)
         if need > len(self.free):
             raise OutOfBlocks()
-        blocks = [self.free.popleft() for _ in range(need)]
-        for b in blocks:
-            self.ref[b] = 1
+        blocks = [self._take() for _ in range(need)]
         sid = self.next_id
         self.next_id += 1
         self.tables[sid] = blocks
         self.lens[sid] = num_tokens
+        self.toks[sid] = None
         return sid
+
+    def add_seq_tokens(self, tokens):
+        """Returns (sid, number of leading tokens whose blocks were shared)."""
+        tokens = [int(t) for t in tokens]
+        n, bs = len(tokens), self.block_size
+        need = -(-n // bs)
+        hits = []
+        for i in range((n - 1) // bs if n > 0 else 0):
+            b = self.cache.get(tuple(tokens[:(i + 1) * bs]))
+            if b is None:
+                break
+            hits.append(b)
+        in_free = sum(1 for b in hits if b in self.free)
+        if need - len(hits) > len(self.free) - in_free:
+            raise OutOfBlocks()
+        for b in hits:
+            if b in self.free:
+                self.free.remove(b)
+            self.ref[b] += 1
+        blocks = hits + [self._take() for _ in range(need - len(hits))]
+        for i in range(len(hits), n // bs):
+            self._register(blocks[i], tuple(tokens[:(i + 1) * bs]))
+        sid = self.next_id
+        self.next_id += 1
+        self.tables[sid] = blocks
+        self.lens[sid] = n
+        self.toks[sid] = tokens
+        return sid, len(hits) * bs
 
     def fork(self, parent: int) -> int:
         blocks = list(self.tables[parent])
@@ -81,10 +139,14 @@ class PoolReplay:
         self.next_id += 1
         self.tables[sid] = blocks
         self.lens[sid] = self.lens[parent]
+        toks = self.toks[parent]
+        self.toks[sid] = None if toks is None else list(toks)
         return sid
 
-    def append_token(self, sid: int):
-        """Returns (slot, pair) where pair is (src, dst) of a copy-on-write or None."""
+    def append_token(self, sid: int, token=None):
+        """Returns (slot, pair) where pair is (src, dst) of a copy-on-write or
+        None.  With a token id a tracked sequence records it and registers the
+        block it fills; without one the sequence stops being tracked."""
         table = self.tables[sid]
         pos = self.lens[sid]
         logical, offset = divmod(pos, self.block_size)
@@ -92,21 +154,27 @@ class PoolReplay:
         if logical == len(table):
             if not self.free:
                 raise OutOfBlocks()
-            b = self.free.popleft()
-            self.ref[b] = 1
+            b = self._take()
             table.append(b)
         else:
             b = table[logical]
             if self.ref[b] > 1:
                 if not self.free:
                     raise OutOfBlocks()
-                nb = self.free.popleft()
-                self.ref[nb] = 1
+                nb = self._take()
                 self.ref[b] -= 1
                 table[logical] = nb
                 pair = (b, nb)
                 b = nb
         self.lens[sid] = pos + 1
+        toks = self.toks[sid]
+        if toks is not None:
+            if token is None:
+                self.toks[sid] = None
+            else:
+                toks.append(int(token))
+                if offset == self.block_size - 1:
+                    self._register(b, tuple(toks[:(logical + 1) * self.block_size]))
         return b * self.block_size + offset, pair
 
     def free_seq(self, sid: int) -> None:
@@ -115,6 +183,11 @@ class PoolReplay:
             if self.ref[b] == 0:
                 self.free.append(b)
         del self.lens[sid]
+        del self.toks[sid]
+
+    def reset_prefix_cache(self) -> None:
+        self.cache.clear()
+        self.block_key.clear()
 
     # -- views -------------------------------------------------------------
     def table(self, sid: int):
@@ -131,6 +204,12 @@ class PoolReplay:
     def num_free(self) -> int:
         return len(self.free)
 
+    def is_cached(self, b: int) -> bool:
+        return b in self.block_key
+
+    def free_queue(self):
+        return list(self.free)
+
     def check_invariants(self) -> None:
         used = [b for b in range(self.num_blocks) if self.ref[b] > 0]
         assert set(used).isdisjoint(self.free), "block both used and free"
@@ -139,3 +218,5 @@ class PoolReplay:
         total_refs = sum(self.ref)
         total_entries = sum(len(t) for t in self.tables.values())
         assert total_refs == total_entries, "ref counts disagree with the tables"
+        for key, b in self.cache.items():
+            assert self.block_key[b] == key and len(key) % self.block_size == 0

@@ -45,7 +45,8 @@ EXPORTS = (
     "pa_pool_add_seq", "pa_pool_fork", "pa_pool_append_token", "pa_pool_append_tokens",
     "pa_pool_free_seq", "pa_pool_block_table", "pa_pool_fill_tables", "pa_pool_slot",
     "pa_pool_ref_count", "pa_pool_num_free", "pa_get_device_error", "pa_status_string",
-    "pa_version", "pa_set_decode_trace",
+    "pa_version", "pa_set_decode_trace", "pa_pool_add_seq_tokens", "pa_pool_append_token_id",
+    "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache",
 )
 
 
@@ -96,6 +97,11 @@ def _load() -> ctypes.CDLL:
         "pa_pool_ref_count": [vp, i32, p_i32],
         "pa_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
         "pa_set_decode_trace": [vp, sz, i32],
+        "pa_pool_add_seq_tokens": [vp, vp, i64, p_i64, p_i64],
+        "pa_pool_append_token_id": [vp, i64, i32, p_i64, vp],
+        "pa_pool_is_cached": [vp, i32, p_i32],
+        "pa_pool_free_queue": [vp, vp, i32, p_i32],
+        "pa_pool_reset_prefix_cache": [vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -372,6 +378,42 @@ class Pool:
 
     def free_seq(self, seq: int) -> None:
         _check(lib.pa_pool_free_seq(self._h, seq), "pa_pool_free_seq")
+
+    # -- prefix caching --------------------------------------------------------
+    def add_seq_tokens(self, tokens):
+        """New sequence from prompt token ids, sharing cached prefix blocks:
+        (seq id, number of leading tokens whose KV is already cached)."""
+        t = torch.tensor([int(x) for x in tokens], dtype=torch.int32)
+        sid = ctypes.c_int64()
+        cached = ctypes.c_int64()
+        _check(lib.pa_pool_add_seq_tokens(self._h, t.data_ptr() if t.numel() else None, t.numel(),
+                                          ctypes.byref(sid), ctypes.byref(cached)),
+               "pa_pool_add_seq_tokens")
+        return sid.value, cached.value
+
+    def append_token_id(self, seq: int, token: int):
+        """append_token that records the token id: (slot, pair or None)."""
+        slot = ctypes.c_int64()
+        pair = (ctypes.c_int64 * 2)()
+        _check(lib.pa_pool_append_token_id(self._h, seq, int(token), ctypes.byref(slot), pair),
+               "pa_pool_append_token_id")
+        return slot.value, (None if pair[0] < 0 else (pair[0], pair[1]))
+
+    def is_cached(self, block: int) -> bool:
+        out = ctypes.c_int32()
+        _check(lib.pa_pool_is_cached(self._h, block, ctypes.byref(out)), "pa_pool_is_cached")
+        return bool(out.value)
+
+    def free_queue(self):
+        """The free queue, front (next handed out) first."""
+        buf = (ctypes.c_int32 * max(self.num_blocks, 1))()
+        n = ctypes.c_int32()
+        _check(lib.pa_pool_free_queue(self._h, buf, self.num_blocks, ctypes.byref(n)),
+               "pa_pool_free_queue")
+        return list(buf[:n.value])
+
+    def reset_prefix_cache(self) -> None:
+        _check(lib.pa_pool_reset_prefix_cache(self._h), "pa_pool_reset_prefix_cache")
 
     def table(self, seq: int):
         n = ctypes.c_int32()

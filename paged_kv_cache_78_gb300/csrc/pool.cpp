@@ -14,10 +14,17 @@
 //     in place;
 //   * freeing drops counts, last block first, and blocks at 0 join the tail
 //     of the FIFO free list.
+// Prefix caching (itan.pw page, section "プレイフィックスキャッシュの詳細"):
+//   * a full block of a sequence created with its token ids carries a chained
+//     hash (the previous block's hash and the block's tokens) and is
+//     registered under it; a partly filled block has none;
+//   * a new request shares the longest run of leading blocks whose hashes are
+//     registered, at most (tokens - 1) / block_size of them; shared blocks
+//     leave the free queue before the request's other blocks are taken;
+//   * freed blocks keep their hash until the free queue hands them out again.
 // Every mutating call either completes or leaves the pool unchanged.
 #include <cstdint>
 #include <cstring>
-#include <deque>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -26,9 +33,89 @@
 
 namespace {
 
+
+// 128-bit chained block hash: two independent 64-bit mixes.
+struct BlockHash {
+  uint64_t a = 0, b = 0;
+  bool operator==(const BlockHash& o) const { return a == o.a && b == o.b; }
+};
+
+struct BlockHashKey {
+  size_t operator()(const BlockHash& h) const { return (size_t)(h.a ^ (h.b * 0x9e3779b97f4a7c15ull)); }
+};
+
+// splitmix64 finaliser (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", 2014).
+inline uint64_t mix64(uint64_t x) {
+  x += 0x9e3779b97f4a7c15ull;
+  x = (x ^ (x >> 30)) * 0xbf58476d1ce4e5b9ull;
+  x = (x ^ (x >> 27)) * 0x94d049bb133111ebull;
+  return x ^ (x >> 31);
+}
+
+// Hash of a block's tokens chained to the previous block's hash.
+BlockHash chain_hash(const BlockHash& prev, const int32_t* tokens, int n) {
+  BlockHash h{prev.a ^ 0x6a09e667f3bcc908ull, prev.b ^ 0xbb67ae8584caa73bull};
+  for (int i = 0; i < n; ++i) {
+    const uint64_t t = (uint64_t)(uint32_t)tokens[i];
+    h.a = mix64(h.a ^ t);
+    h.b = mix64(h.b + (t << 1 | 1) * 0xd6e8feb86659fd93ull);
+  }
+  h.a = mix64(h.a ^ (uint64_t)n);
+  h.b = mix64(h.b ^ ((uint64_t)n << 32));
+  return h;
+}
+
+// Free blocks as a doubly linked queue over the block ids: taken from the
+// front, returned to the back, and a cached block that a new request shares
+// leaves it from wherever it is.
+struct FreeQueue {
+  std::vector<int32_t> prev, next;
+  std::vector<char> in;
+  int32_t head = -1, tail = -1;
+  int32_t count = 0;
+
+  void init(int32_t n) {
+    prev.assign((size_t)n, -1);
+    next.assign((size_t)n, -1);
+    in.assign((size_t)n, 0);
+  }
+  bool empty() const { return count == 0; }
+  size_t size() const { return (size_t)count; }
+  int32_t front() const { return head; }
+  void push_back(int32_t b) {
+    prev[b] = tail;
+    next[b] = -1;
+    if (tail >= 0) next[tail] = b; else head = b;
+    tail = b;
+    in[b] = 1;
+    ++count;
+  }
+  void push_front(int32_t b) {
+    next[b] = head;
+    prev[b] = -1;
+    if (head >= 0) prev[head] = b; else tail = b;
+    head = b;
+    in[b] = 1;
+    ++count;
+  }
+  void remove(int32_t b) {
+    if (prev[b] >= 0) next[prev[b]] = next[b]; else head = next[b];
+    if (next[b] >= 0) prev[next[b]] = prev[b]; else tail = prev[b];
+    prev[b] = next[b] = -1;
+    in[b] = 0;
+    --count;
+  }
+  void pop_front() { remove(head); }
+};
+
 struct Seq {
   std::vector<int32_t> blocks;  // logical block i -> physical block
   int64_t len = 0;              // tokens written
+  bool tracked = false;         // created with token ids (takes part in prefix caching)
+  std::vector<int32_t> tokens;  // tracked: every token id so far
+  BlockHash chain;              // tracked: chained hash of the full blocks so far
+  int64_t chained = 0;          // tracked: how many full blocks `chain` covers
 };
 
 // One reversible step of append_token, kept for rollback.
@@ -37,6 +124,8 @@ struct AppendUndo {
   int kind;          // 0: filled an existing private block, 1: new block, 2: copy-on-write
   int32_t old_block; // kind 2: the shared block the sequence left
   int32_t new_block; // kind 1 and 2: the block taken from the free list
+  bool had_hash;     // kind 1 and 2: new_block was registered before it was taken
+  BlockHash hash;    //   ... under this hash
 };
 
 }  // namespace
@@ -45,9 +134,37 @@ struct pa_pool {
   int32_t num_blocks = 0;
   int32_t block_size = 0;
   std::vector<int32_t> ref;
-  std::deque<int32_t> free_list;
+  FreeQueue free_list;
   std::unordered_map<int64_t, Seq> seqs;
   int64_t next_id = 0;
+  // Prefix cache: registered full blocks by chained hash, and each block's hash.
+  std::unordered_map<BlockHash, int32_t, BlockHashKey> cached;
+  std::vector<BlockHash> block_hash;
+  std::vector<char> hashed;
+
+  void uncache(int32_t b) {
+    if (!hashed[b]) return;
+    auto it = cached.find(block_hash[b]);
+    if (it != cached.end() && it->second == b) cached.erase(it);
+    hashed[b] = 0;
+  }
+
+  // Register block b (full, of a tracked sequence) under h unless another
+  // block already holds that hash.
+  void register_block(int32_t b, const BlockHash& h) {
+    if (hashed[b] || cached.count(h)) return;
+    cached.emplace(h, b);
+    block_hash[b] = h;
+    hashed[b] = 1;
+  }
+
+  // Chained hash of logical block i of a tracked sequence (its tokens known).
+  BlockHash hash_of(const Seq& s, int64_t i) const {
+    BlockHash h;
+    for (int64_t j = 0; j <= i; ++j)
+      h = chain_hash(h, s.tokens.data() + j * block_size, block_size);
+    return h;
+  }
 
   Seq* find(int64_t id) {
     auto it = seqs.find(id);
@@ -58,16 +175,32 @@ struct pa_pool {
     return it == seqs.end() ? nullptr : &it->second;
   }
 
-  int32_t take_free() {
+  // A block handed out for new content loses its cached hash (reported in
+  // *had / *h so that a rollback can restore it).
+  int32_t take_free(bool* had = nullptr, BlockHash* h = nullptr) {
     int32_t b = free_list.front();
     free_list.pop_front();
+    if (had) *had = hashed[b] != 0;
+    if (h) *h = block_hash[b];
+    uncache(b);
     ref[b] = 1;
     return b;
   }
 
-  // Reserve the next token's slot of `s` (id `id`).  Returns PA_OK or
-  // PA_ERR_OUT_OF_BLOCKS with nothing changed.
-  pa_status append(int64_t id, Seq& s, int64_t* slot, int64_t pair[2], AppendUndo* undo) {
+  // A tracked sequence whose block `logical` just became full: chain its hash
+  // and register the block.
+  void seal(Seq& s, int64_t logical) {
+    if (!s.tracked || logical != s.chained) return;
+    s.chain = chain_hash(s.chain, s.tokens.data() + logical * block_size, block_size);
+    s.chained = logical + 1;
+    register_block(s.blocks[(size_t)logical], s.chain);
+  }
+
+  // Reserve the next token's slot of `s` (id `id`); `token` is its id, or
+  // null (a tracked sequence then stops taking part in prefix caching).
+  // Returns PA_OK or PA_ERR_OUT_OF_BLOCKS with nothing changed.
+  pa_status append(int64_t id, Seq& s, const int32_t* token, int64_t* slot, int64_t pair[2],
+                   AppendUndo* undo) {
     const int64_t pos = s.len;
     const int64_t logical = pos / block_size;
     const int64_t offset = pos % block_size;
@@ -75,42 +208,59 @@ struct pa_pool {
     int32_t b;
     if (logical == (int64_t)s.blocks.size()) {
       if (free_list.empty()) return PA_ERR_OUT_OF_BLOCKS;
-      b = take_free();
+      *undo = {id, 1, -1, -1, false, BlockHash{}};
+      b = take_free(&undo->had_hash, &undo->hash);
+      undo->new_block = b;
       s.blocks.push_back(b);
-      *undo = {id, 1, -1, b};
     } else {
       b = s.blocks[(size_t)logical];
       if (ref[b] > 1) {
         if (free_list.empty()) return PA_ERR_OUT_OF_BLOCKS;
-        int32_t nb = take_free();
+        *undo = {id, 2, b, -1, false, BlockHash{}};
+        int32_t nb = take_free(&undo->had_hash, &undo->hash);
+        undo->new_block = nb;
         ref[b] -= 1;
         s.blocks[(size_t)logical] = nb;
         pair[0] = b;
         pair[1] = nb;
-        *undo = {id, 2, b, nb};
         b = nb;
       } else {
-        *undo = {id, 0, -1, -1};
+        *undo = {id, 0, -1, -1, false, BlockHash{}};
       }
     }
     s.len = pos + 1;
     *slot = (int64_t)b * block_size + offset;
+    if (s.tracked && token) {
+      s.tokens.push_back(*token);
+      if (offset == block_size - 1) seal(s, logical);
+    }
     return PA_OK;
   }
 
+  // A tracked sequence appended to without a token id (after the append
+  // succeeded): it stops taking part in prefix caching.
+  static void untrack(Seq& s) {
+    if (!s.tracked) return;
+    s.tracked = false;
+    s.tokens.clear();
+    s.tokens.shrink_to_fit();
+  }
+
+  // Undo an untracked append (the batch call appends without token ids).
   void rollback(const AppendUndo& u) {
     Seq& s = seqs[u.seq];
     s.len -= 1;
     if (u.kind == 1) {
       s.blocks.pop_back();
-      ref[u.new_block] = 0;
-      free_list.push_front(u.new_block);
     } else if (u.kind == 2) {
       const int64_t logical = s.len / block_size;
       s.blocks[(size_t)logical] = u.old_block;
       ref[u.old_block] += 1;
+    }
+    if (u.kind != 0) {
       ref[u.new_block] = 0;
       free_list.push_front(u.new_block);
+      if (u.had_hash) register_block(u.new_block, u.hash);
     }
   }
 };
@@ -126,6 +276,9 @@ pa_status pa_pool_create(int32_t num_blocks, int32_t block_size, const int32_t* 
   p->num_blocks = num_blocks;
   p->block_size = block_size;
   p->ref.assign((size_t)num_blocks, 0);
+  p->free_list.init(num_blocks);
+  p->block_hash.assign((size_t)num_blocks, BlockHash{});
+  p->hashed.assign((size_t)num_blocks, 0);
   if (free_order) {
     std::vector<char> seen((size_t)num_blocks, 0);
     for (int32_t i = 0; i < num_blocks; ++i) {
@@ -177,7 +330,91 @@ pa_status pa_pool_append_token(pa_pool* pool, int64_t seq, int64_t* slot, int64_
   Seq* s = pool->find(seq);
   if (!s) return PA_ERR_BAD_STATE;
   AppendUndo undo;
-  return pool->append(seq, *s, slot, cow_pair, &undo);
+  const pa_status st = pool->append(seq, *s, nullptr, slot, cow_pair, &undo);
+  if (st == PA_OK) pa_pool::untrack(*s);
+  return st;
+}
+
+pa_status pa_pool_append_token_id(pa_pool* pool, int64_t seq, int32_t token, int64_t* slot,
+                                  int64_t cow_pair[2]) {
+  if (!pool || !slot || !cow_pair) return PA_ERR_INVALID_ARG;
+  Seq* s = pool->find(seq);
+  if (!s) return PA_ERR_BAD_STATE;
+  AppendUndo undo;
+  return pool->append(seq, *s, &token, slot, cow_pair, &undo);
+}
+
+pa_status pa_pool_add_seq_tokens(pa_pool* pool, const int32_t* tokens, int64_t num_tokens,
+                                 int64_t* seq_id, int64_t* num_cached_tokens) {
+  if (!pool || !seq_id || !num_cached_tokens || num_tokens < 0 || (num_tokens > 0 && !tokens))
+    return PA_ERR_INVALID_ARG;
+  const int32_t bs = pool->block_size;
+  const int64_t need = (num_tokens + bs - 1) / bs;
+  const int64_t full = num_tokens / bs;
+  // The longest run of leading full blocks already registered, at most
+  // (num_tokens - 1) / block_size: the last token is always computed.
+  const int64_t max_hit = num_tokens > 0 ? (num_tokens - 1) / bs : 0;
+  std::vector<int32_t> hit;
+  std::vector<BlockHash> chain;
+  chain.reserve((size_t)full);
+  BlockHash h;
+  for (int64_t i = 0; i < full; ++i) {
+    h = chain_hash(h, tokens + i * bs, bs);
+    chain.push_back(h);
+  }
+  for (int64_t i = 0; i < max_hit; ++i) {
+    auto it = pool->cached.find(chain[(size_t)i]);
+    if (it == pool->cached.end()) break;
+    hit.push_back(it->second);
+  }
+  int64_t hits_in_queue = 0;
+  for (int32_t b : hit) hits_in_queue += pool->free_list.in[b] ? 1 : 0;
+  if (need - (int64_t)hit.size() > (int64_t)pool->free_list.size() - hits_in_queue)
+    return PA_ERR_OUT_OF_BLOCKS;
+  Seq s;
+  s.blocks.reserve((size_t)need);
+  // Shared blocks first leave the free queue, then the rest are taken.
+  for (int32_t b : hit) {
+    if (pool->free_list.in[b]) pool->free_list.remove(b);
+    pool->ref[b] += 1;
+    s.blocks.push_back(b);
+  }
+  for (int64_t i = (int64_t)hit.size(); i < need; ++i) s.blocks.push_back(pool->take_free());
+  s.len = num_tokens;
+  s.tracked = true;
+  s.tokens.assign(tokens, tokens + num_tokens);
+  // Register the new full blocks (their KV is the caller's to write).
+  for (int64_t i = (int64_t)hit.size(); i < full; ++i)
+    pool->register_block(s.blocks[(size_t)i], chain[(size_t)i]);
+  s.chain = full > 0 ? chain[(size_t)full - 1] : BlockHash{};
+  s.chained = full;
+  const int64_t id = pool->next_id++;
+  pool->seqs.emplace(id, std::move(s));
+  *seq_id = id;
+  *num_cached_tokens = (int64_t)hit.size() * bs;
+  return PA_OK;
+}
+
+pa_status pa_pool_is_cached(const pa_pool* pool, int32_t block, int32_t* cached) {
+  if (!pool || !cached || block < 0 || block >= pool->num_blocks) return PA_ERR_INVALID_ARG;
+  *cached = pool->hashed[(size_t)block] ? 1 : 0;
+  return PA_OK;
+}
+
+pa_status pa_pool_free_queue(const pa_pool* pool, int32_t* out, int32_t cap, int32_t* n) {
+  if (!pool || !n || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID_ARG;
+  int32_t i = 0;
+  for (int32_t b = pool->free_list.head; b >= 0; b = pool->free_list.next[(size_t)b], ++i)
+    if (i < cap) out[i] = b;
+  *n = i;
+  return i > cap ? PA_ERR_INVALID_ARG : PA_OK;
+}
+
+pa_status pa_pool_reset_prefix_cache(pa_pool* pool) {
+  if (!pool) return PA_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < pool->num_blocks; ++b) pool->hashed[(size_t)b] = 0;
+  pool->cached.clear();
+  return PA_OK;
 }
 
 pa_status pa_pool_append_tokens(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* slots,
@@ -192,7 +429,7 @@ pa_status pa_pool_append_tokens(pa_pool* pool, const int64_t* seqs, int32_t n, i
   for (int32_t i = 0; i < n; ++i) {
     int64_t pair[2];
     AppendUndo undo;
-    pa_status st = pool->append(seqs[i], *pool->find(seqs[i]), &slots[i], pair, &undo);
+    pa_status st = pool->append(seqs[i], *pool->find(seqs[i]), nullptr, &slots[i], pair, &undo);
     if (st != PA_OK) {
       for (auto it = done.rbegin(); it != done.rend(); ++it) pool->rollback(*it);
       *num_pairs = 0;
@@ -205,6 +442,7 @@ pa_status pa_pool_append_tokens(pa_pool* pool, const int64_t* seqs, int32_t n, i
       ++npairs;
     }
   }
+  for (int32_t i = 0; i < n; ++i) pa_pool::untrack(*pool->find(seqs[i]));
   *num_pairs = npairs;
   return PA_OK;
 }

@@ -62,6 +62,73 @@ def test_allocation_example_matches_pages():
     assert pool.table(sid)[0] == g["after_full"]["table"] and slot == g["after_full"]["slot"]
 
 
+def _prefix_timeline(pool):
+    """Drive `pool` (the library's or the oracle's) through the pages' prefix
+    cache timeline and check every state the page states."""
+    g = golden("prefix_cache_example.json")
+    r0, cached = pool.add_seq_tokens(g["t1"]["tokens"])
+    assert cached == g["t1"]["num_cached_tokens"]
+    assert pool.table(r0)[0] == g["t1"]["table"]
+    assert [b for b in range(g["num_blocks"]) if pool.is_cached(b)] == g["t1"]["cached_blocks"]
+    for t in g["t2"]["append"]:
+        pool.append_token(r0, t) if isinstance(pool, PoolReplay) else pool.append_token_id(r0, t)
+    assert pool.table(r0)[0] == g["t2"]["table"]
+    assert [b for b in range(g["num_blocks"]) if pool.is_cached(b)] == g["t2"]["cached_blocks"]
+    r1, cached = pool.add_seq_tokens(g["t3"]["tokens"])
+    assert cached == g["t3"]["num_cached_tokens"]
+    assert pool.table(r1)[0] == g["t3"]["table"]
+    refs = pool.ref if isinstance(pool, PoolReplay) else None
+    for b, r in g["t3"]["refs"].items():
+        assert (refs[int(b)] if refs else pool.ref_count(int(b))) == r
+    pool.free_seq(r0)
+    assert pool.free_queue() == g["t4"]["free_queue"]
+    assert all(pool.is_cached(b) for b in g["t4"]["still_cached"])
+    pool.free_seq(r1)
+    assert pool.free_queue() == g["t5"]["free_queue"]
+    r2, cached = pool.add_seq_tokens(g["t6"]["tokens"])
+    assert cached == g["t6"]["num_cached_tokens"]
+    assert pool.table(r2)[0] == g["t6"]["table"]
+    assert pool.free_queue() == g["t6"]["free_queue"]
+    return pool
+
+
+def test_prefix_cache_timeline_matches_pages():
+    g = golden("prefix_cache_example.json")
+    pool = _prefix_timeline(pa.Pool(g["num_blocks"], g["block_size"]))
+    assert not pool.is_cached(3)  # reused for request 2's partial last block: its hash is gone
+
+
+def test_prefix_cache_timeline_matches_pages_in_the_oracle_replay():
+    g = golden("prefix_cache_example.json")
+    pool = _prefix_timeline(PoolReplay(g["num_blocks"], g["block_size"]))
+    pool.check_invariants()
+    assert not pool.is_cached(3)
+
+
+def test_prefix_cache_never_shares_the_last_prompt_token():
+    pool = pa.Pool(16, 4)
+    a, _ = pool.add_seq_tokens(range(8))         # two full blocks, both registered
+    b, cached = pool.add_seq_tokens(range(8))    # same 8 tokens: only (8 - 1) // 4 = 1 block shared
+    assert cached == 4
+    assert pool.table(b)[0][0] == pool.table(a)[0][0] and pool.table(b)[0][1] != pool.table(a)[0][1]
+    c, cached = pool.add_seq_tokens(list(range(8)) + [99])
+    assert cached == 8 and pool.table(c)[0][:2] == pool.table(a)[0]
+    d, cached = pool.add_seq_tokens([1] + list(range(1, 9)))  # differs in the first token
+    assert cached == 0
+
+
+def test_prefix_cache_out_of_blocks_changes_nothing():
+    pool = pa.Pool(5, 4)
+    a, _ = pool.add_seq_tokens(range(12))        # blocks 0,1,2
+    pool.free_seq(a)                             # queue 3 4 2 1 0, all three cached
+    before = pool.free_queue()
+    with pytest.raises(pa.OutOfBlocks):
+        pool.add_seq_tokens(list(range(12)) + list(range(100, 112)))  # 3 shared + 3 new > 5
+    assert pool.free_queue() == before and all(pool.is_cached(b) for b in (0, 1, 2))
+    b, cached = pool.add_seq_tokens(list(range(12)) + [7])
+    assert cached == 12 and pool.free_queue() == [4]  # 3 shared + one new block (3)
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_random_operations_match_replay(seed):
     rng = np.random.default_rng(seed)
@@ -69,9 +136,36 @@ def test_random_operations_match_replay(seed):
     order = rng.permutation(nb)
     ours, ref = pa.Pool(nb, bs, order), PoolReplay(nb, bs, order)
     live = []
+    prompts = [[int(t) for t in rng.integers(0, 3, size=24)] for _ in range(4)]
     for step in range(1500):
-        op = int(rng.integers(0, 5))
-        if op == 0 or not live:
+        op = int(rng.integers(0, 8))
+        if op == 5 and live:
+            # prefix caching: prompts drawn as prefixes of a few shared streams
+            base = prompts[int(rng.integers(len(prompts)))]
+            toks = base[:int(rng.integers(0, len(base) + 1))] + \
+                [int(t) for t in rng.integers(0, 3, size=int(rng.integers(0, 3)))]
+            try:
+                want = ref.add_seq_tokens(toks)
+            except OutOfBlocks:
+                with pytest.raises(pa.OutOfBlocks):
+                    ours.add_seq_tokens(toks)
+                continue
+            assert ours.add_seq_tokens(toks) == want
+            live.append(want[0])
+        elif op == 6 and live:
+            sid = live[int(rng.integers(len(live)))]
+            tok = int(rng.integers(0, 3))
+            try:
+                want = ref.append_token(sid, tok)
+            except OutOfBlocks:
+                with pytest.raises(pa.OutOfBlocks):
+                    ours.append_token_id(sid, tok)
+                continue
+            assert ours.append_token_id(sid, tok) == want
+        elif op == 7 and step % 97 == 0:
+            ref.reset_prefix_cache()
+            ours.reset_prefix_cache()
+        elif op == 0 or not live:
             n = int(rng.integers(0, 14))
             try:
                 want = ref.add_seq(n)
@@ -100,10 +194,13 @@ def test_random_operations_match_replay(seed):
             ref.free_seq(sid)
             ours.free_seq(sid)
         assert ours.num_free() == ref.num_free()
+        assert ours.free_queue() == ref.free_queue()
         for sid in live:
             assert ours.table(sid) == ref.table(sid)
         for b in range(nb):
             assert ours.ref_count(b) == ref.ref[b]
+            assert ours.is_cached(b) == ref.is_cached(b)
+        ref.check_invariants()
 
 
 def test_batch_append_is_all_or_nothing():
