@@ -66,6 +66,31 @@ def make_workload(name: str):
 WORKLOAD_PARTITION = {"long_context": 512, "long_context_mixed": 512}
 
 
+# The largest length each workload's statement allows (what a contiguous
+# max-length preallocation reserves per sequence).
+WORKLOAD_MAX_LEN = {"qwen2_gqa": 2048, "long_context": 32768, "long_context_mixed": 131072}
+
+
+def memory_report(pa, case, workload: str) -> dict:
+    """KV memory the workload's sequences leave allocated but unused: paged
+    (the library's host pool, block sizes 8/16/32; the waste sits in each
+    sequence's last block) against reserving the largest allowed length per
+    sequence in one contiguous region."""
+    lens = [int(n) for n in case.seq_lens]
+    max_len = WORKLOAD_MAX_LEN.get(workload, 2048)
+    paged = {}
+    for bs in (8, 16, 32):
+        pool = pa.Pool(sum(-(-n // bs) for n in lens) + 1, bs)
+        for n in lens:
+            pool.add_seq(n)
+        tokens, blocks = pool.usage()
+        paged[str(bs)] = {"waste": round(1.0 - tokens / max(1, blocks * bs), 5),
+                          "unused_slots_per_seq": round((blocks * bs - tokens) / len(lens), 2)}
+    used = sum(lens)
+    return {"paged": paged, "contiguous_reserved_len": max_len,
+            "contiguous_waste": round(1.0 - used / (len(lens) * max_len), 5)}
+
+
 def step_bytes(case, partition: int = 0) -> dict:
     """Algorithmic bytes of one step: what the operations must read and write
     once.  With split-KV partitions, each sequence of more than one partition
@@ -582,6 +607,8 @@ def main():
 
     import torch
 
+    import paged_kv_cache_78_gb300 as pa
+
     if world > 1:
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local_rank)
@@ -649,6 +676,7 @@ def main():
         },
         "e2e": e2e,
         "paging": r["paging"],
+        "memory": memory_report(pa, case, args.workload),
         "clocks": r["clocks"],
         "cpu_baseline": cpu,
     }

@@ -292,6 +292,14 @@ pa_status pa_pool_fill_tables(const pa_pool* pool, const int64_t* seqs, int32_t 
 pa_status pa_pool_slot(const pa_pool* pool, int64_t seq, int64_t pos, int64_t* slot);
 pa_status pa_pool_ref_count(const pa_pool* pool, int32_t block, int32_t* ref);
 int32_t pa_pool_num_free(const pa_pool* pool);
+/* Memory use: *tokens = sum of the live sequences' lengths, *blocks_in_use =
+ * physical blocks with a reference.  Without sharing, the KV slots allocated
+ * but unused are blocks_in_use * block_size - tokens, all of them in
+ * sequences' last blocks (studying-code.tistory.com/16, section "물리적 블록
+ * 할당": the waste of a request stays within one block; tech.blogsailing.com/
+ * ?p=100, section 2: on average BLOCK_SIZE / 2 per sequence).  Shared blocks
+ * count once in blocks_in_use and once per sequence in tokens. */
+pa_status pa_pool_usage(const pa_pool* pool, int64_t* tokens, int64_t* blocks_in_use);
 
 /* ---------------------------------------------------------------------------
  * Prefix caching on the pool (itan.pw "vLLMにおけるKVCacheマネージャーの詳細

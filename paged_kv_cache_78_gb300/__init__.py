@@ -46,7 +46,7 @@ EXPORTS = (
     "pa_pool_free_seq", "pa_pool_block_table", "pa_pool_fill_tables", "pa_pool_slot",
     "pa_pool_ref_count", "pa_pool_num_free", "pa_get_device_error", "pa_status_string",
     "pa_version", "pa_set_decode_trace", "pa_pool_add_seq_tokens", "pa_pool_append_token_id",
-    "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache",
+    "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache", "pa_pool_usage",
 )
 
 
@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
         "pa_pool_is_cached": [vp, i32, p_i32],
         "pa_pool_free_queue": [vp, vp, i32, p_i32],
         "pa_pool_reset_prefix_cache": [vp],
+        "pa_pool_usage": [vp, p_i64, p_i64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -411,6 +412,12 @@ class Pool:
         _check(lib.pa_pool_free_queue(self._h, buf, self.num_blocks, ctypes.byref(n)),
                "pa_pool_free_queue")
         return list(buf[:n.value])
+
+    def usage(self):
+        """(tokens held by live sequences, physical blocks in use)."""
+        t, b = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.pa_pool_usage(self._h, ctypes.byref(t), ctypes.byref(b)), "pa_pool_usage")
+        return t.value, b.value
 
     def reset_prefix_cache(self) -> None:
         _check(lib.pa_pool_reset_prefix_cache(self._h), "pa_pool_reset_prefix_cache")

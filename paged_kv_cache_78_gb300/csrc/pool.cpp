@@ -513,6 +513,16 @@ pa_status pa_pool_ref_count(const pa_pool* pool, int32_t block, int32_t* ref) {
   return PA_OK;
 }
 
+pa_status pa_pool_usage(const pa_pool* pool, int64_t* tokens, int64_t* blocks_in_use) {
+  if (!pool || !tokens || !blocks_in_use) return PA_ERR_INVALID_ARG;
+  int64_t t = 0, b = 0;
+  for (const auto& kv : pool->seqs) t += kv.second.len;
+  for (int32_t i = 0; i < pool->num_blocks; ++i) b += pool->ref[(size_t)i] > 0 ? 1 : 0;
+  *tokens = t;
+  *blocks_in_use = b;
+  return PA_OK;
+}
+
 int32_t pa_pool_num_free(const pa_pool* pool) {
   return pool ? (int32_t)pool->free_list.size() : -1;
 }

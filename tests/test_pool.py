@@ -279,3 +279,19 @@ def test_pool_errors():
         pool.free_seq(0)
     with pytest.raises(pa.PAError):
         pa.Pool(4, 4, [0, 1, 1, 2])
+
+
+def test_usage_counts_tokens_and_blocks():
+    pool = pa.Pool(32, 16)
+    a = pool.add_seq(50)            # 4 blocks, 14 slots unused in the last
+    assert pool.usage() == (50, 4)
+    b = pool.fork(a)                # shared blocks count once, tokens per sequence
+    assert pool.usage() == (100, 4)
+    pool.append_token(b)            # copy-on-write of the partly filled last block
+    assert pool.usage() == (101, 5)
+    pool.free_seq(a)
+    assert pool.usage() == (51, 4)
+    # waste stays within the last block: at most block_size - 1 slots per sequence
+    c = pool.add_seq(33)
+    tokens, blocks = pool.usage()
+    assert blocks * 16 - tokens == (64 - 51) + (48 - 33)
