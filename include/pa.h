@@ -107,6 +107,26 @@ pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* 
                          int32_t num_pairs, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Swap block copies between two pools of the same block geometry (block
+ * size, KV heads, head size, dtype; the block counts may differ): for each
+ * pair i, block pairs[2i] of src_cache is copied to block pairs[2i+1] of
+ * dst_cache, keys and values, bit-exactly.  The pages' swapping moves a
+ * preempted sequence's blocks to CPU memory and back
+ * (studying-code.tistory.com/16, section "스와핑(Swapping)").  One of the
+ * pools is normally the GPU pool and the other a CPU pool in page-locked
+ * host memory, which the kernel reads or writes directly (over NVLink-C2C on
+ * GB300).  Each of dst_cache, src_cache and pairs must be device memory or
+ * page-locked host memory; pageable host memory returns PA_ERR_INVALID_ARG
+ * and launches nothing.  pairs: int64 [num_pairs][2] (pa_pool_swap_out /
+ * pa_pool_swap_in give them).  An id outside its pool skips the pair and
+ * records PA_DEVERR_BLOCK_ID.  Asynchronous on `stream`: the host pool may
+ * be reused only after the stream has passed the copy.
+ * ------------------------------------------------------------------------- */
+pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const void* src_cache,
+                         const pa_cache_desc* src_desc, const int64_t* pairs, int32_t num_pairs,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
  * Paged decode attention: one query token per sequence against the
  * sequence's cached tokens, block by block through its block table
  * (studying-code.tistory.com/16, section "PagedAttention: 운영체제의 페이징
@@ -292,14 +312,47 @@ pa_status pa_pool_fill_tables(const pa_pool* pool, const int64_t* seqs, int32_t 
 pa_status pa_pool_slot(const pa_pool* pool, int64_t seq, int64_t pos, int64_t* slot);
 pa_status pa_pool_ref_count(const pa_pool* pool, int32_t block, int32_t* ref);
 int32_t pa_pool_num_free(const pa_pool* pool);
-/* Memory use: *tokens = sum of the live sequences' lengths, *blocks_in_use =
- * physical blocks with a reference.  Without sharing, the KV slots allocated
+/* Memory use: *tokens = sum of the GPU-resident sequences' lengths,
+ * *blocks_in_use = physical blocks with a reference.  Without sharing, the KV slots allocated
  * but unused are blocks_in_use * block_size - tokens, all of them in
  * sequences' last blocks (studying-code.tistory.com/16, section "물리적 블록
  * 할당": the waste of a request stays within one block; tech.blogsailing.com/
  * ?p=100, section 2: on average BLOCK_SIZE / 2 per sequence).  Shared blocks
  * count once in blocks_in_use and once per sequence in tokens. */
 pa_status pa_pool_usage(const pa_pool* pool, int64_t* tokens, int64_t* blocks_in_use);
+
+/* ---------------------------------------------------------------------------
+ * Swapping (studying-code.tistory.com/16, sections "All-or-Nothing Eviction"
+ * and "스와핑(Swapping)": a preempted sequence group leaves the GPU whole, its
+ * blocks go to a CPU block allocator whose size never exceeds the GPU's
+ * block count, and come back when the GPU has room).
+ *   pa_pool_set_cpu_blocks: size the CPU region (0 <= n <= num_blocks; only
+ *     while no sequence is swapped out); its free list starts as 0..n-1.
+ *   pa_pool_swap_out: move every block of the n sequences to CPU blocks,
+ *     taken from the front of the CPU free list in first-use order (sequences
+ *     in the given order, blocks in table order; a block shared inside the
+ *     group moves once and keeps its count).  pairs (room for [blocks][2])
+ *     receive (GPU block, CPU block) for pa_swap_blocks(cpu pool <- gpu
+ *     pool), *num_pairs their number.  The GPU blocks are then released like
+ *     pa_pool_free_seq (each sequence's last block first, to the tail of the
+ *     free queue; cached prefix blocks stay cached).  PA_ERR_BAD_STATE if a
+ *     sequence is unknown or already swapped, or a block is also held by a
+ *     sequence outside the group; PA_ERR_OUT_OF_BLOCKS if the CPU region is
+ *     too small; either way nothing changes.
+ *   pa_pool_swap_in: the reverse, GPU blocks from the front of the free
+ *     queue, pairs (CPU block, GPU block) for pa_swap_blocks(gpu pool <- cpu
+ *     pool).
+ *   A swapped-out sequence has no slots and no GPU table: append, fork,
+ *   fill_tables and slot return PA_ERR_BAD_STATE; pa_pool_block_table gives
+ *   its CPU block ids; pa_pool_free_seq releases its CPU blocks.
+ * ------------------------------------------------------------------------- */
+pa_status pa_pool_set_cpu_blocks(pa_pool* pool, int32_t num_cpu_blocks);
+pa_status pa_pool_swap_out(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* pairs,
+                           int32_t* num_pairs);
+pa_status pa_pool_swap_in(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* pairs,
+                          int32_t* num_pairs);
+pa_status pa_pool_is_swapped(const pa_pool* pool, int64_t seq, int32_t* swapped);
+int32_t pa_pool_num_free_cpu(const pa_pool* pool);
 
 /* ---------------------------------------------------------------------------
  * Prefix caching on the pool (itan.pw "vLLMにおけるKVCacheマネージャーの詳細

@@ -49,6 +49,18 @@ the key instead of a chained hash:
   rest of the request (time 6 of the page's timeline);
 * freed blocks stay registered until the free queue hands them out again
   (time 4: blocks 2 and 3 are free and still cached).
+
+Swapping (studying-code.tistory.com/16, sections "All-or-Nothing Eviction"
+and "스와핑(Swapping)"):
+
+* a preempted sequence group leaves the GPU whole: every block of its
+  sequences is copied to a block of a CPU allocator whose size never exceeds
+  the GPU's block count, then the GPU blocks are released; a block shared
+  with a sequence outside the group cannot leave (the group would be split);
+* swapping in takes GPU blocks for the group's CPU blocks and releases those;
+* the order of the copies (first use, sequences in the given order, blocks
+  in table order) and of the releases (each sequence's last block first, to
+  the tail of the free list) follows the rest of this replay.
 """
 from __future__ import annotations
 
@@ -56,6 +68,10 @@ from collections import deque
 
 
 class OutOfBlocks(Exception):
+    pass
+
+
+class BadState(Exception):
     pass
 
 
@@ -74,6 +90,9 @@ class PoolReplay:
         self.lens: dict[int, int] = {}
         self.next_id = 0
         self.toks: dict[int, list[int] | None] = {}  # token ids of tracked sequences
+        self.cpu_free: deque = deque()
+        self.cpu_ref: list[int] = []
+        self.swapped: set[int] = set()
         self.cache: dict[tuple, int] = {}            # token prefix -> registered block
         self.block_key: dict[int, tuple] = {}        # registered block -> its prefix
 
@@ -132,6 +151,8 @@ class PoolReplay:
         return sid, len(hits) * bs
 
     def fork(self, parent: int) -> int:
+        if parent in self.swapped:
+            raise BadState()
         blocks = list(self.tables[parent])
         for b in blocks:
             self.ref[b] += 1
@@ -147,6 +168,8 @@ class PoolReplay:
         """Returns (slot, pair) where pair is (src, dst) of a copy-on-write or
         None.  With a token id a tracked sequence records it and registers the
         block it fills; without one the sequence stops being tracked."""
+        if sid in self.swapped:
+            raise BadState()
         table = self.tables[sid]
         pos = self.lens[sid]
         logical, offset = divmod(pos, self.block_size)
@@ -178,12 +201,69 @@ class PoolReplay:
         return b * self.block_size + offset, pair
 
     def free_seq(self, sid: int) -> None:
+        swapped = sid in self.swapped
+        ref, free = (self.cpu_ref, self.cpu_free) if swapped else (self.ref, self.free)
         for b in reversed(self.tables.pop(sid)):
-            self.ref[b] -= 1
-            if self.ref[b] == 0:
-                self.free.append(b)
+            ref[b] -= 1
+            if ref[b] == 0:
+                free.append(b)
         del self.lens[sid]
         del self.toks[sid]
+        self.swapped.discard(sid)
+
+    # -- swapping ------------------------------------------------------------
+    def set_cpu_blocks(self, n: int) -> None:
+        if n < 0 or n > self.num_blocks:
+            raise ValueError("the CPU region may not exceed the GPU block count")
+        if self.swapped:
+            raise BadState()
+        self.cpu_free = deque(range(n))
+        self.cpu_ref = [0] * n
+
+    def _move(self, sids, out: bool):
+        if len(set(sids)) != len(sids):
+            raise ValueError("sequence listed twice")
+        for sid in sids:
+            if sid not in self.tables or (sid in self.swapped) == out:
+                raise BadState()
+        src_ref = self.ref if out else self.cpu_ref
+        dst_free = self.cpu_free if out else self.free
+        uses: dict[int, int] = {}
+        for sid in sids:
+            for b in self.tables[sid]:
+                uses[b] = uses.get(b, 0) + 1
+        if any(uses[b] != src_ref[b] for b in uses):
+            raise BadState()
+        if len(uses) > len(dst_free):
+            raise OutOfBlocks()
+        where, pairs = {}, []
+        for b in uses:  # dicts keep first-use order
+            if out:
+                d = self.cpu_free.popleft()
+                self.cpu_ref[d] = self.ref[b]
+            else:
+                r = self.cpu_ref[b]
+                d = self._take()
+                self.ref[d] = r
+            where[b] = d
+            pairs.append((b, d))
+        for sid in sids:
+            for b in reversed(self.tables[sid]):
+                src_ref[b] -= 1
+                if src_ref[b] == 0:
+                    (self.free if out else self.cpu_free).append(b)
+            self.tables[sid] = [where[b] for b in self.tables[sid]]
+            if out:
+                self.swapped.add(sid)
+            else:
+                self.swapped.discard(sid)
+        return pairs
+
+    def swap_out(self, sids):
+        return self._move(list(sids), True)
+
+    def swap_in(self, sids):
+        return self._move(list(sids), False)
 
     def reset_prefix_cache(self) -> None:
         self.cache.clear()
@@ -212,11 +292,15 @@ class PoolReplay:
 
     def check_invariants(self) -> None:
         used = [b for b in range(self.num_blocks) if self.ref[b] > 0]
+        cpu_used = [b for b in range(len(self.cpu_ref)) if self.cpu_ref[b] > 0]
+        assert len(cpu_used) + len(self.cpu_free) == len(self.cpu_ref), "CPU block lost"
+        assert set(cpu_used).isdisjoint(self.cpu_free), "CPU block both used and free"
+        assert sum(self.cpu_ref) == sum(len(self.tables[s]) for s in self.swapped)
         assert set(used).isdisjoint(self.free), "block both used and free"
         assert len(used) + len(self.free) == self.num_blocks, "block lost"
         assert len(set(self.free)) == len(self.free), "block twice in the free list"
         total_refs = sum(self.ref)
-        total_entries = sum(len(t) for t in self.tables.values())
+        total_entries = sum(len(t) for s, t in self.tables.items() if s not in self.swapped)
         assert total_refs == total_entries, "ref counts disagree with the tables"
         for key, b in self.cache.items():
             assert self.block_key[b] == key and len(key) % self.block_size == 0

@@ -47,6 +47,8 @@ EXPORTS = (
     "pa_pool_ref_count", "pa_pool_num_free", "pa_get_device_error", "pa_status_string",
     "pa_version", "pa_set_decode_trace", "pa_pool_add_seq_tokens", "pa_pool_append_token_id",
     "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache", "pa_pool_usage",
+    "pa_swap_blocks", "pa_pool_set_cpu_blocks", "pa_pool_swap_out", "pa_pool_swap_in",
+    "pa_pool_is_swapped", "pa_pool_num_free_cpu",
 )
 
 
@@ -103,6 +105,11 @@ def _load() -> ctypes.CDLL:
         "pa_pool_free_queue": [vp, vp, i32, p_i32],
         "pa_pool_reset_prefix_cache": [vp],
         "pa_pool_usage": [vp, p_i64, p_i64],
+        "pa_swap_blocks": [vp, desc, vp, desc, vp, i32, vp],
+        "pa_pool_set_cpu_blocks": [vp, i32],
+        "pa_pool_swap_out": [vp, vp, i32, vp, p_i32],
+        "pa_pool_swap_in": [vp, vp, i32, vp, p_i32],
+        "pa_pool_is_swapped": [vp, i64, p_i32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -209,6 +216,30 @@ def pa_copy_blocks(cache: torch.Tensor, pairs: torch.Tensor, stream=None) -> Non
     _check(lib.pa_copy_blocks(_dev_ptr(cache, "cache"), ctypes.byref(desc),
                               _dev_ptr(pairs, "pairs", torch.int64) if n else None, n,
                               _stream(stream)), "pa_copy_blocks")
+
+
+def _dev_or_pinned_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("%s must be a CUDA tensor or page-locked host memory" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def pa_swap_blocks(dst_cache: torch.Tensor, src_cache: torch.Tensor, pairs: torch.Tensor,
+                   stream=None) -> None:
+    """Copy block pairs[i, 0] of src_cache to block pairs[i, 1] of dst_cache
+    (keys and values); either pool may be page-locked host memory."""
+    n = pairs.shape[0] if pairs.numel() else 0
+    if n and (pairs.dim() != 2 or pairs.shape[1] != 2):
+        raise ValueError("pairs must be [num_pairs, 2]")
+    dd, sd = cache_desc(dst_cache), cache_desc(src_cache)
+    _check(lib.pa_swap_blocks(_dev_or_pinned_ptr(dst_cache, "dst_cache"), ctypes.byref(dd),
+                              _dev_or_pinned_ptr(src_cache, "src_cache"), ctypes.byref(sd),
+                              _dev_or_pinned_ptr(pairs, "pairs", torch.int64) if n else None, n,
+                              _stream(stream)), "pa_swap_blocks")
 
 
 def pa_decode_partition_size(cache_or_desc, num_seqs: int, num_heads: int, max_seq_len: int,
@@ -418,6 +449,36 @@ class Pool:
         t, b = ctypes.c_int64(), ctypes.c_int64()
         _check(lib.pa_pool_usage(self._h, ctypes.byref(t), ctypes.byref(b)), "pa_pool_usage")
         return t.value, b.value
+
+    # -- swapping ---------------------------------------------------------------
+    def set_cpu_blocks(self, n: int) -> None:
+        _check(lib.pa_pool_set_cpu_blocks(self._h, n), "pa_pool_set_cpu_blocks")
+        self.num_cpu_blocks = n
+
+    def _swap(self, fn, name, seqs):
+        s = torch.tensor([int(x) for x in seqs], dtype=torch.int64)
+        cap = max(1, self.num_blocks)
+        pairs = torch.empty((cap, 2), dtype=torch.int64)
+        k = ctypes.c_int32()
+        _check(fn(self._h, s.data_ptr() if s.numel() else None, s.numel(), pairs.data_ptr(),
+                  ctypes.byref(k)), name)
+        return pairs[:k.value].clone()
+
+    def swap_out(self, seqs):
+        """Move a sequence group to CPU blocks: int64 [k, 2] (GPU block, CPU block) pairs."""
+        return self._swap(lib.pa_pool_swap_out, "pa_pool_swap_out", seqs)
+
+    def swap_in(self, seqs):
+        """Move a swapped group back: int64 [k, 2] (CPU block, GPU block) pairs."""
+        return self._swap(lib.pa_pool_swap_in, "pa_pool_swap_in", seqs)
+
+    def is_swapped(self, seq: int) -> bool:
+        out = ctypes.c_int32()
+        _check(lib.pa_pool_is_swapped(self._h, seq, ctypes.byref(out)), "pa_pool_is_swapped")
+        return bool(out.value)
+
+    def num_free_cpu(self) -> int:
+        return int(lib.pa_pool_num_free_cpu(self._h))
 
     def reset_prefix_cache(self) -> None:
         _check(lib.pa_pool_reset_prefix_cache(self._h), "pa_pool_reset_prefix_cache")

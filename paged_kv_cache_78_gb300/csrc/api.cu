@@ -263,10 +263,60 @@ pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* 
   if ((st = device_state(&err, nullptr)) != PA_OK) return st;
   const int64_t block_bytes = (int64_t)desc->block_size * desc->num_kv_heads * desc->head_size *
                               elem_bytes(desc->dtype);
-  const int64_t plane_bytes = block_bytes * desc->num_blocks;
-  return cuda_status(pa::launch_copy_blocks(cache, pairs, num_pairs, desc->num_blocks,
-                                            block_bytes, plane_bytes, err,
+  return cuda_status(pa::launch_copy_blocks(cache, cache, pairs, num_pairs, desc->num_blocks,
+                                            desc->num_blocks, block_bytes, err,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+// The address a kernel uses for `p`: device memory as is, page-locked host
+// memory through its device mapping; anything else (pageable host memory)
+// is refused.
+static pa_status kernel_address(const void* p, const void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return PA_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+    *out = a.devicePointer;
+    return PA_OK;
+  }
+  return PA_ERR_INVALID_ARG;
+}
+
+pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const void* src_cache,
+                         const pa_cache_desc* src_desc, const int64_t* pairs, int32_t num_pairs,
+                         void* stream) {
+  pa_status st = check_desc(dst_desc);
+  if (st != PA_OK) return st;
+  if ((st = check_desc(src_desc)) != PA_OK) return st;
+  if (dst_desc->block_size != src_desc->block_size ||
+      dst_desc->num_kv_heads != src_desc->num_kv_heads ||
+      dst_desc->head_size != src_desc->head_size || dst_desc->dtype != src_desc->dtype)
+    return PA_ERR_INVALID_ARG;
+  if (num_pairs < 0 || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!dst_cache || !src_cache || !pairs || !aligned(dst_cache, 16) || !aligned(src_cache, 16) ||
+      !aligned(pairs, 8))
+    return PA_ERR_INVALID_ARG;
+  const void* d = nullptr;
+  const void* s = nullptr;
+  const void* pr = nullptr;
+  if ((st = kernel_address(dst_cache, &d)) != PA_OK) return st;
+  if ((st = kernel_address(src_cache, &s)) != PA_OK) return st;
+  if ((st = kernel_address(pairs, &pr)) != PA_OK) return st;
+  unsigned int* err = nullptr;
+  if ((st = device_state(&err, nullptr)) != PA_OK) return st;
+  const int64_t block_bytes = (int64_t)dst_desc->block_size * dst_desc->num_kv_heads *
+                              dst_desc->head_size * elem_bytes(dst_desc->dtype);
+  return cuda_status(pa::launch_copy_blocks(const_cast<void*>(d), s,
+                                            static_cast<const int64_t*>(pr), num_pairs,
+                                            dst_desc->num_blocks, src_desc->num_blocks,
+                                            block_bytes, err, static_cast<cudaStream_t>(stream)));
 }
 
 pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,

@@ -42,24 +42,29 @@ __global__ void reshape_and_cache_kernel(uint8_t* __restrict__ cache,
   stg_v4(dst, ldg_nc_v4(src));
 }
 
-// One CTA per (pair, K or V, slice of the block): block src -> block dst,
-// copied whole (studying-code.tistory.com/16, section "생성 단계에서의
-// Copy-on-Write": the writer of a shared block copies its content to a new block).
-__global__ void copy_blocks_kernel(uint8_t* __restrict__ cache, const int64_t* __restrict__ pairs,
-                                   int64_t num_blocks, int64_t block_bytes, int64_t plane_bytes,
-                                   unsigned int* err) {
+// One CTA per (pair, K or V, slice of the block): block src of the source
+// pool -> block dst of the destination pool, copied whole.  Copy-on-write
+// copies within one pool (studying-code.tistory.com/16, section "생성 단계에서의
+// Copy-on-Write": the writer of a shared block copies its content to a new
+// block); swapping copies between the GPU pool and a CPU pool of the same
+// block geometry (same page, section "스와핑(Swapping)").
+__global__ void copy_blocks_kernel(uint8_t* __restrict__ dst_cache,
+                                   const uint8_t* __restrict__ src_cache,
+                                   const int64_t* __restrict__ pairs, int64_t dst_blocks,
+                                   int64_t src_blocks, int64_t block_bytes, int64_t dst_plane,
+                                   int64_t src_plane, unsigned int* err) {
   grid_dependents_launch();
   grid_dependency_wait();
   const int pair = blockIdx.x >> 1;
   const int kv = blockIdx.x & 1;
   const int64_t src = __ldg(pairs + 2 * pair);
   const int64_t dst = __ldg(pairs + 2 * pair + 1);
-  if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks) {
+  if (src < 0 || dst < 0 || src >= src_blocks || dst >= dst_blocks) {
     if (kv == 0 && blockIdx.y == 0 && threadIdx.x == 0) record_error(err, PA_DEVERR_BLOCK_ID);
     return;
   }
-  const uint8_t* s = cache + kv * plane_bytes + src * block_bytes;
-  uint8_t* d = cache + kv * plane_bytes + dst * block_bytes;
+  const uint8_t* s = src_cache + kv * src_plane + src * block_bytes;
+  uint8_t* d = dst_cache + kv * dst_plane + dst * block_bytes;
   const int64_t n16 = block_bytes / 16;
   const int64_t step = (int64_t)gridDim.y * blockDim.x;
   int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x;
@@ -94,17 +99,20 @@ cudaError_t launch_reshape_and_cache(void* cache, const void* key, const void* v
                            dim3(block), 0, stream, args);
 }
 
-cudaError_t launch_copy_blocks(void* cache, const int64_t* pairs, int num_pairs,
-                               int64_t num_blocks, int64_t block_bytes, int64_t plane_bytes,
-                               unsigned int* err, cudaStream_t stream) {
+cudaError_t launch_copy_blocks(void* dst_cache, const void* src_cache, const int64_t* pairs,
+                               int num_pairs, int64_t dst_blocks, int64_t src_blocks,
+                               int64_t block_bytes, unsigned int* err, cudaStream_t stream) {
   const int block = 256;
   const int64_t per_cta = (int64_t)block * 16 * 8;  // about 8 vectors per thread
   int slices = (int)((block_bytes + per_cta - 1) / per_cta);
   if (slices < 1) slices = 1;
   if (slices > 1024) slices = 1024;
   dim3 grid((unsigned)num_pairs * 2u, (unsigned)slices);
-  uint8_t* c = static_cast<uint8_t*>(cache);
-  void* args[] = {&c, &pairs, &num_blocks, &block_bytes, &plane_bytes, &err};
+  uint8_t* d = static_cast<uint8_t*>(dst_cache);
+  const uint8_t* s = static_cast<const uint8_t*>(src_cache);
+  int64_t dst_plane = dst_blocks * block_bytes, src_plane = src_blocks * block_bytes;
+  void* args[] = {&d, &s, &pairs, &dst_blocks, &src_blocks, &block_bytes, &dst_plane, &src_plane,
+                  &err};
   return launch_overlapped((const void*)copy_blocks_kernel, grid, dim3(block), 0, stream, args);
 }
 

@@ -33,9 +33,10 @@ cudaError_t launch_reshape_and_cache(void* cache, const void* key, const void* v
                                      int64_t num_slots, int row_bytes, int64_t plane_bytes,
                                      unsigned int* err, cudaStream_t stream);
 
-cudaError_t launch_copy_blocks(void* cache, const int64_t* pairs, int num_pairs,
-                               int64_t num_blocks, int64_t block_bytes, int64_t plane_bytes,
-                               unsigned int* err, cudaStream_t stream);
+// Block copies from src_cache to dst_cache (the same pool for copy-on-write).
+cudaError_t launch_copy_blocks(void* dst_cache, const void* src_cache, const int64_t* pairs,
+                               int num_pairs, int64_t dst_blocks, int64_t src_blocks,
+                               int64_t block_bytes, unsigned int* err, cudaStream_t stream);
 
 // Decode launchers, one per element type.  `supported` is set to false (and
 // nothing launched) when no kernel exists for (head_size, group).

@@ -25,6 +25,7 @@
 // Every mutating call either completes or leaves the pool unchanged.
 #include <cstdint>
 #include <cstring>
+#include <deque>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -116,6 +117,7 @@ struct Seq {
   std::vector<int32_t> tokens;  // tracked: every token id so far
   BlockHash chain;              // tracked: chained hash of the full blocks so far
   int64_t chained = 0;          // tracked: how many full blocks `chain` covers
+  bool swapped = false;         // blocks are CPU block ids (swapped out)
 };
 
 // One reversible step of append_token, kept for rollback.
@@ -137,6 +139,10 @@ struct pa_pool {
   FreeQueue free_list;
   std::unordered_map<int64_t, Seq> seqs;
   int64_t next_id = 0;
+  // CPU swap region: blocks 0..num_cpu_blocks-1, a FIFO free list and counts.
+  int32_t num_cpu_blocks = 0;
+  std::vector<int32_t> cpu_ref;
+  std::deque<int32_t> cpu_free;
   // Prefix cache: registered full blocks by chained hash, and each block's hash.
   std::unordered_map<BlockHash, int32_t, BlockHashKey> cached;
   std::vector<BlockHash> block_hash;
@@ -316,7 +322,7 @@ pa_status pa_pool_add_seq(pa_pool* pool, int64_t num_tokens, int64_t* seq_id) {
 pa_status pa_pool_fork(pa_pool* pool, int64_t parent, int64_t* child) {
   if (!pool || !child) return PA_ERR_INVALID_ARG;
   const Seq* p = pool->find(parent);
-  if (!p) return PA_ERR_BAD_STATE;
+  if (!p || p->swapped) return PA_ERR_BAD_STATE;
   Seq c = *p;
   for (int32_t b : c.blocks) pool->ref[b] += 1;
   const int64_t id = pool->next_id++;
@@ -328,7 +334,7 @@ pa_status pa_pool_fork(pa_pool* pool, int64_t parent, int64_t* child) {
 pa_status pa_pool_append_token(pa_pool* pool, int64_t seq, int64_t* slot, int64_t cow_pair[2]) {
   if (!pool || !slot || !cow_pair) return PA_ERR_INVALID_ARG;
   Seq* s = pool->find(seq);
-  if (!s) return PA_ERR_BAD_STATE;
+  if (!s || s->swapped) return PA_ERR_BAD_STATE;
   AppendUndo undo;
   const pa_status st = pool->append(seq, *s, nullptr, slot, cow_pair, &undo);
   if (st == PA_OK) pa_pool::untrack(*s);
@@ -339,7 +345,7 @@ pa_status pa_pool_append_token_id(pa_pool* pool, int64_t seq, int32_t token, int
                                   int64_t cow_pair[2]) {
   if (!pool || !slot || !cow_pair) return PA_ERR_INVALID_ARG;
   Seq* s = pool->find(seq);
-  if (!s) return PA_ERR_BAD_STATE;
+  if (!s || s->swapped) return PA_ERR_BAD_STATE;
   AppendUndo undo;
   return pool->append(seq, *s, &token, slot, cow_pair, &undo);
 }
@@ -422,7 +428,7 @@ pa_status pa_pool_append_tokens(pa_pool* pool, const int64_t* seqs, int32_t n, i
   if (!pool || n < 0 || (n > 0 && (!seqs || !slots || !cow_pairs)) || !num_pairs)
     return PA_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n; ++i)
-    if (!pool->find(seqs[i])) return PA_ERR_BAD_STATE;
+    if (!pool->find(seqs[i]) || pool->find(seqs[i])->swapped) return PA_ERR_BAD_STATE;
   std::vector<AppendUndo> done;
   done.reserve((size_t)n);
   int32_t npairs = 0;
@@ -452,11 +458,14 @@ pa_status pa_pool_free_seq(pa_pool* pool, int64_t seq) {
   auto it = pool->seqs.find(seq);
   if (it == pool->seqs.end()) return PA_ERR_BAD_STATE;
   const std::vector<int32_t>& blocks = it->second.blocks;
+  std::vector<int32_t>& ref = it->second.swapped ? pool->cpu_ref : pool->ref;
   for (auto b = blocks.rbegin(); b != blocks.rend(); ++b) {
-    if (pool->ref[*b] <= 0) return PA_ERR_BAD_STATE;  // cannot happen unless corrupted
+    if (ref[*b] <= 0) return PA_ERR_BAD_STATE;  // cannot happen unless corrupted
   }
   for (auto b = blocks.rbegin(); b != blocks.rend(); ++b) {
-    if (--pool->ref[*b] == 0) pool->free_list.push_back(*b);
+    if (--ref[*b] == 0) {
+      if (it->second.swapped) pool->cpu_free.push_back(*b); else pool->free_list.push_back(*b);
+    }
   }
   pool->seqs.erase(it);
   return PA_OK;
@@ -482,7 +491,7 @@ pa_status pa_pool_fill_tables(const pa_pool* pool, const int64_t* seqs, int32_t 
     return PA_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n; ++i) {
     const Seq* s = pool->find(seqs[i]);
-    if (!s) return PA_ERR_BAD_STATE;
+    if (!s || s->swapped) return PA_ERR_BAD_STATE;
     if ((int64_t)s->blocks.size() > max_blocks_per_seq || s->len > INT32_MAX)
       return PA_ERR_INVALID_ARG;
   }
@@ -500,7 +509,7 @@ pa_status pa_pool_fill_tables(const pa_pool* pool, const int64_t* seqs, int32_t 
 pa_status pa_pool_slot(const pa_pool* pool, int64_t seq, int64_t pos, int64_t* slot) {
   if (!pool || !slot) return PA_ERR_INVALID_ARG;
   const Seq* s = pool->find(seq);
-  if (!s) return PA_ERR_BAD_STATE;
+  if (!s || s->swapped) return PA_ERR_BAD_STATE;
   if (pos < 0 || pos >= s->len) return PA_ERR_INVALID_ARG;
   *slot = (int64_t)s->blocks[(size_t)(pos / pool->block_size)] * pool->block_size +
           pos % pool->block_size;
@@ -513,10 +522,103 @@ pa_status pa_pool_ref_count(const pa_pool* pool, int32_t block, int32_t* ref) {
   return PA_OK;
 }
 
+pa_status pa_pool_set_cpu_blocks(pa_pool* pool, int32_t num_cpu_blocks) {
+  if (!pool || num_cpu_blocks < 0 || num_cpu_blocks > pool->num_blocks) return PA_ERR_INVALID_ARG;
+  for (const auto& kv : pool->seqs)
+    if (kv.second.swapped) return PA_ERR_BAD_STATE;
+  pool->num_cpu_blocks = num_cpu_blocks;
+  pool->cpu_ref.assign((size_t)num_cpu_blocks, 0);
+  pool->cpu_free.clear();
+  for (int32_t b = 0; b < num_cpu_blocks; ++b) pool->cpu_free.push_back(b);
+  return PA_OK;
+}
+
+// Swap a sequence group between GPU and CPU blocks (all or nothing).  `out`
+// selects the direction; pairs receive (src, dst) block ids in first-use
+// order, one per distinct block.
+static pa_status swap_group(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* pairs,
+                            int32_t* num_pairs, bool out) {
+  if (!pool || n < 0 || (n > 0 && (!seqs || !pairs)) || !num_pairs) return PA_ERR_INVALID_ARG;
+  *num_pairs = 0;
+  std::vector<Seq*> group;
+  for (int32_t i = 0; i < n; ++i) {
+    Seq* s = pool->find(seqs[i]);
+    if (!s || s->swapped == out) return PA_ERR_BAD_STATE;
+    for (Seq* g : group)
+      if (g == s) return PA_ERR_INVALID_ARG;  // listed twice
+    group.push_back(s);
+  }
+  std::vector<int32_t>& from_ref = out ? pool->ref : pool->cpu_ref;
+  // Distinct source blocks in first-use order, and the group's references.
+  std::unordered_map<int32_t, int32_t> uses;
+  std::vector<int32_t> order;
+  for (Seq* s : group)
+    for (int32_t b : s->blocks)
+      if (uses[b]++ == 0) order.push_back(b);
+  // A block also held outside the group would be split: refuse.
+  for (int32_t b : order)
+    if (uses[b] != from_ref[(size_t)b]) return PA_ERR_BAD_STATE;
+  const size_t avail = out ? pool->cpu_free.size() : pool->free_list.size();
+  if (order.size() > avail) return PA_ERR_OUT_OF_BLOCKS;
+  std::unordered_map<int32_t, int32_t> to;
+  for (size_t i = 0; i < order.size(); ++i) {
+    const int32_t b = order[i];
+    int32_t d;
+    if (out) {
+      d = pool->cpu_free.front();
+      pool->cpu_free.pop_front();
+      pool->cpu_ref[(size_t)d] = pool->ref[(size_t)b];
+    } else {
+      const int32_t r = pool->cpu_ref[(size_t)b];
+      d = pool->take_free();
+      pool->ref[(size_t)d] = r;
+    }
+    to[b] = d;
+    pairs[2 * i] = b;
+    pairs[2 * i + 1] = d;
+  }
+  // Release the source blocks, each sequence's last block first, and move
+  // the tables to the destination blocks.
+  for (Seq* s : group) {
+    for (auto it = s->blocks.rbegin(); it != s->blocks.rend(); ++it) {
+      if (--from_ref[(size_t)*it] == 0) {
+        if (out) pool->free_list.push_back(*it); else pool->cpu_free.push_back(*it);
+      }
+    }
+    for (int32_t& b : s->blocks) b = to[b];
+    s->swapped = out;
+  }
+  *num_pairs = (int32_t)order.size();
+  return PA_OK;
+}
+
+pa_status pa_pool_swap_out(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* pairs,
+                           int32_t* num_pairs) {
+  return swap_group(pool, seqs, n, pairs, num_pairs, true);
+}
+
+pa_status pa_pool_swap_in(pa_pool* pool, const int64_t* seqs, int32_t n, int64_t* pairs,
+                          int32_t* num_pairs) {
+  return swap_group(pool, seqs, n, pairs, num_pairs, false);
+}
+
+pa_status pa_pool_is_swapped(const pa_pool* pool, int64_t seq, int32_t* swapped) {
+  if (!pool || !swapped) return PA_ERR_INVALID_ARG;
+  const Seq* s = pool->find(seq);
+  if (!s) return PA_ERR_BAD_STATE;
+  *swapped = s->swapped ? 1 : 0;
+  return PA_OK;
+}
+
+int32_t pa_pool_num_free_cpu(const pa_pool* pool) {
+  return pool ? (int32_t)pool->cpu_free.size() : -1;
+}
+
 pa_status pa_pool_usage(const pa_pool* pool, int64_t* tokens, int64_t* blocks_in_use) {
   if (!pool || !tokens || !blocks_in_use) return PA_ERR_INVALID_ARG;
   int64_t t = 0, b = 0;
-  for (const auto& kv : pool->seqs) t += kv.second.len;
+  for (const auto& kv : pool->seqs)
+    if (!kv.second.swapped) t += kv.second.len;
   for (int32_t i = 0; i < pool->num_blocks; ++i) b += pool->ref[(size_t)i] > 0 ? 1 : 0;
   *tokens = t;
   *blocks_in_use = b;

@@ -1,6 +1,8 @@
 """GPU parity of the cache write and the copy-on-write block copy: bit-exact
 against the oracle, including padding slots, untouched bytes and ids outside
 the pool (skipped and recorded, never faulting)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -92,3 +94,65 @@ def test_zero_token_and_zero_pair_calls():
     pa.pa_reshape_and_cache(cache, empty, empty, torch.empty(0, dtype=torch.int64, device="cuda"))
     pa.pa_copy_blocks(cache, torch.empty((0, 2), dtype=torch.int64, device="cuda"))
     assert not cache.any()
+
+
+def _pinned_like(rng, shape, dtype):
+    host = workloads.garbage_values(rng, shape, dtype)
+    if dtype == "bf16":
+        t = torch.from_numpy(host.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(host)
+    return host, t.pin_memory()
+
+
+def _host_bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 \
+        else t.numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("dtype,nb,ncpu,bs,hkv,d", [
+    ("bf16", 64, 32, 16, 2, 64),
+    ("bf16", 40, 40, 8, 8, 128),
+    ("fp32", 24, 12, 4, 4, 64),
+])
+def test_swap_round_trip_bit_exact(dtype, nb, ncpu, bs, hkv, d):
+    # A sequence group leaves the GPU for page-locked host blocks and comes
+    # back to other GPU blocks; every byte matches a plain block assignment
+    # and CPU blocks outside the pairs keep their canary bytes.
+    rng = np.random.default_rng(nb + ncpu + d)
+    gpu_host = workloads.garbage_values(rng, (2, nb, bs, hkv, d), dtype)
+    gpu = to_device(gpu_host)
+    cpu_ref, cpu = _pinned_like(rng, (2, ncpu, bs, hkv, d), dtype)
+    pool = pa.Pool(nb, bs)
+    pool.set_cpu_blocks(ncpu)
+    a = pool.add_seq(3 * bs + 1)
+    a2 = pool.fork(a)
+    pool.add_seq(2 * bs)                              # another request keeps its blocks
+    out = pool.swap_out([a, a2])                      # (GPU block, CPU block)
+    for pairs in (out.cuda(), out.pin_memory()):      # pair lists on the device or pinned
+        pa.pa_swap_blocks(cpu, gpu, pairs)
+        torch.cuda.synchronize()
+        expect = cpu_ref.copy()
+        expect[:, out[:, 1].numpy()] = gpu_host[:, out[:, 0].numpy()]
+        assert np.array_equal(_host_bits(cpu), bits(expect))
+    back = pool.swap_in([a, a2])                      # (CPU block, GPU block)
+    assert sorted(back[:, 0].tolist()) == sorted(out[:, 1].tolist())
+    pa.pa_swap_blocks(gpu, cpu, back.cuda())
+    torch.cuda.synchronize()
+    now = to_host_bits(gpu)
+    old_of_new = {int(c): int(g) for g, c in out.tolist()}
+    for c, g in back.tolist():
+        assert np.array_equal(bits(now[:, g]), bits(gpu_host[:, old_of_new[c]]))
+    assert pa.pa_get_device_error() == 0
+
+
+def test_swap_refuses_pageable_host_memory():
+    cache = torch.zeros((2, 4, 4, 2, 64), dtype=torch.bfloat16, device="cuda")
+    pageable = torch.zeros((2, 4, 4, 2, 64), dtype=torch.bfloat16)
+    pairs = torch.tensor([[0, 1]], dtype=torch.int64, device="cuda")
+    desc = pa.cache_desc(cache)
+    st = pa.lib.pa_swap_blocks(pageable.data_ptr(), ctypes.byref(desc), cache.data_ptr(),
+                               ctypes.byref(desc), pairs.data_ptr(), 1, None)
+    assert st == pa.PA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0

@@ -11,7 +11,7 @@ import torch
 import oracle
 import paged_kv_cache_78_gb300 as pa
 import workloads
-from oracle.pool_replay import OutOfBlocks, PoolReplay
+from oracle.pool_replay import BadState, OutOfBlocks, PoolReplay
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -135,7 +135,11 @@ def test_random_operations_match_replay(seed):
     nb, bs = 40, 4
     order = rng.permutation(nb)
     ours, ref = pa.Pool(nb, bs, order), PoolReplay(nb, bs, order)
+    ours.set_cpu_blocks(nb // 2)
+    ref.set_cpu_blocks(nb // 2)
     live = []
+    resident = lambda: [x for x in live if x not in ref.swapped]
+    pick = lambda xs: xs[int(rng.integers(len(xs)))]
     prompts = [[int(t) for t in rng.integers(0, 3, size=24)] for _ in range(4)]
     for step in range(1500):
         op = int(rng.integers(0, 8))
@@ -152,8 +156,8 @@ def test_random_operations_match_replay(seed):
                 continue
             assert ours.add_seq_tokens(toks) == want
             live.append(want[0])
-        elif op == 6 and live:
-            sid = live[int(rng.integers(len(live)))]
+        elif op == 6 and resident():
+            sid = pick(resident())
             tok = int(rng.integers(0, 3))
             try:
                 want = ref.append_token(sid, tok)
@@ -165,6 +169,26 @@ def test_random_operations_match_replay(seed):
         elif op == 7 and step % 97 == 0:
             ref.reset_prefix_cache()
             ours.reset_prefix_cache()
+        elif op == 7 and live:
+            # swap a sequence group out (all sequences sharing blocks with one) or back in
+            sid = live[int(rng.integers(len(live)))]
+            out = not ref.tables[sid] or sid not in ref.swapped
+            group, frontier = {sid}, [sid]
+            while frontier:
+                x = frontier.pop()
+                for y in live:
+                    if y not in group and (y in ref.swapped) == (x in ref.swapped) and \
+                            set(ref.tables[y]) & set(ref.tables[x]):
+                        group.add(y)
+                        frontier.append(y)
+            group = sorted(group)
+            try:
+                want = ref.swap_out(group) if out else ref.swap_in(group)
+            except (OutOfBlocks, BadState) as exc:
+                with pytest.raises(pa.OutOfBlocks if isinstance(exc, OutOfBlocks) else pa.PAError):
+                    ours.swap_out(group) if out else ours.swap_in(group)
+                continue
+            assert _pairs(ours.swap_out(group) if out else ours.swap_in(group)) == want
         elif op == 0 or not live:
             n = int(rng.integers(0, 14))
             try:
@@ -175,13 +199,13 @@ def test_random_operations_match_replay(seed):
                 continue
             assert ours.add_seq(n) == want
             live.append(want)
-        elif op == 1:
-            p = live[int(rng.integers(len(live)))]
+        elif op == 1 and resident():
+            p = pick(resident())
             want = ref.fork(p)
             assert ours.fork(p) == want
             live.append(want)
-        elif op in (2, 3):
-            sid = live[int(rng.integers(len(live)))]
+        elif op in (2, 3) and resident():
+            sid = pick(resident())
             try:
                 want = ref.append_token(sid)
             except OutOfBlocks:
@@ -189,11 +213,12 @@ def test_random_operations_match_replay(seed):
                     ours.append_token(sid)
                 continue
             assert ours.append_token(sid) == want
-        else:
+        elif op == 4:
             sid = live.pop(int(rng.integers(len(live))))
             ref.free_seq(sid)
             ours.free_seq(sid)
         assert ours.num_free() == ref.num_free()
+        assert ours.num_free_cpu() == len(ref.cpu_free)
         assert ours.free_queue() == ref.free_queue()
         for sid in live:
             assert ours.table(sid) == ref.table(sid)
@@ -295,3 +320,61 @@ def test_usage_counts_tokens_and_blocks():
     c = pool.add_seq(33)
     tokens, blocks = pool.usage()
     assert blocks * 16 - tokens == (64 - 51) + (48 - 33)
+
+
+
+def _pairs(t):
+    return [tuple(int(x) for x in row) for row in t.tolist()]
+
+
+def test_swap_preempts_a_sequence_group_whole():
+    # Two samples of one request share a prompt; a second request needs the
+    # GPU blocks, so the group is swapped out whole, and back in after.
+    ours, ref = pa.Pool(8, 4), PoolReplay(8, 4)
+    for p in (ours, ref):
+        p.set_cpu_blocks(8)
+    a = ours.add_seq(10); assert ref.add_seq(10) == a          # blocks 0,1,2 (2 tokens in 2)
+    a2 = ours.fork(a); assert ref.fork(a) == a2
+    b = ours.add_seq(16); assert ref.add_seq(16) == b          # blocks 3..6; one block left
+    with pytest.raises(pa.PAError) as e:
+        ours.swap_out([a])                                      # would split the group
+    assert e.value.status == pa.PA_ERR_BAD_STATE
+    got = _pairs(ours.swap_out([a, a2]))
+    assert got == ref.swap_out([a, a2]) == [(0, 0), (1, 1), (2, 2)]
+    assert ours.num_free() == ref.num_free() == 4 and ours.num_free_cpu() == 5
+    assert ours.is_swapped(a) and ours.table(a)[0] == ref.table(a)[0] == [0, 1, 2]
+    for call in (lambda: ours.append_token(a), lambda: ours.fork(a2),
+                 lambda: ours.fill_tables([a], 8), lambda: ours.slot(a, 0)):
+        with pytest.raises(pa.PAError) as e:
+            call()
+        assert e.value.status == pa.PA_ERR_BAD_STATE
+    for _ in range(5):                                          # the other request grows
+        assert ours.append_token(b) == ref.append_token(b)
+    ours.free_seq(b); ref.free_seq(b)
+    got = _pairs(ours.swap_in([a2, a]))
+    assert got == ref.swap_in([a2, a])
+    assert ours.table(a) == ref.table(a) and ours.table(a2) == ref.table(a2)
+    assert all(ours.ref_count(x) == 2 for x in ours.table(a)[0])
+    slot, pair = ours.append_token(a2)                          # copy-on-write still works
+    assert (slot, pair) == ref.append_token(a2) and pair is not None
+    assert ours.num_free_cpu() == 8
+    ref.check_invariants()
+
+
+def test_swap_limits():
+    pool = pa.Pool(6, 4)
+    with pytest.raises(pa.PAError) as e:
+        pool.set_cpu_blocks(7)                                  # never more than the GPU has
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    pool.set_cpu_blocks(2)
+    a = pool.add_seq(12)
+    with pytest.raises(pa.OutOfBlocks):
+        pool.swap_out([a])                                      # 3 blocks, 2 CPU blocks
+    assert not pool.is_swapped(a) and pool.num_free() == 3 and pool.num_free_cpu() == 2
+    b = pool.add_seq(8)
+    pool.swap_out([b])
+    with pytest.raises(pa.PAError) as e:
+        pool.set_cpu_blocks(4)                                  # not while swapped
+    assert e.value.status == pa.PA_ERR_BAD_STATE
+    pool.free_seq(b)                                            # frees its CPU blocks
+    assert pool.num_free_cpu() == 2 and pool.num_free() == 3
