@@ -58,7 +58,46 @@ def make_workload(name: str):
         return workloads.long_context(mixed=True)
     if name == "tiny":
         return workloads.tiny()
+    if name in ("shared_prefix_fork", "shared_prefix_prefix"):
+        return shared_prefix_case(name[len("shared_prefix_"):])
     raise SystemExit("unknown workload %s" % name)
+
+
+def shared_prefix_case(variant: str):
+    """The shared-prefix / parallel-sampling batch: the seeded pool script
+    (16 requests of a 1018-token prompt forked into 8 samples with 1-64 private
+    tokens each, or 128 requests forked from one 512-token prefix with 64-512
+    private tokens) replayed on the library's host pool, so forks share blocks
+    by reference count and a write into a shared, partly filled block moves
+    the writer to a copy.  K/V are drawn once per physical slot and gathered
+    per sequence, so every sequence sharing a block sees the same rows."""
+    import paged_kv_cache_78_gb300 as pa
+
+    script = workloads.shared_prefix_script(variant=variant)
+    pool = pa.Pool(script.num_blocks, script.block_size, script.free_order)
+    for kind, arg in script.ops:
+        if kind == "add":
+            pool.add_seq(arg)
+        elif kind == "fork":
+            pool.fork(arg)
+        else:
+            pool.append_token(arg)
+    seqs = script.decode_seqs
+    mb = max(len(pool.table(x)[0]) for x in seqs)
+    bt, sl = pool.fill_tables(seqs, mb)
+    bt, sl = bt.numpy().astype(np.int32), sl.numpy().astype(np.int32)
+    hq, hkv, d, bs, nb = 32, 8, 128, script.block_size, script.num_blocks
+    rng = np.random.default_rng([3, 9, int(variant == "fork")])
+    slot_k = workloads.random_values(rng, (nb * bs, hkv, d), "bf16")
+    slot_v = workloads.random_values(rng, (nb * bs, hkv, d), "bf16")
+    idx = np.concatenate([bt[r, np.arange(n) // bs].astype(np.int64) * bs + np.arange(n) % bs
+                          for r, n in enumerate(sl)])
+    starts = np.zeros(len(seqs) + 1, dtype=np.int64)
+    starts[1:] = np.cumsum(sl.astype(np.int64))
+    q = workloads.random_values(rng, (len(seqs), hq, d), "bf16")
+    return workloads.DecodeCase("shared_prefix_" + variant, 3, hq, hkv, d, bs, nb, "bf16",
+                                1.0 / math.sqrt(d), sl, bt, q, slot_k[idx], slot_v[idx], starts,
+                                meta={"unique_slots": int(np.unique(idx).size)})
 
 
 # Workloads whose statement fixes the split-KV partition (512-token partitions
@@ -68,7 +107,8 @@ WORKLOAD_PARTITION = {"long_context": 512, "long_context_mixed": 512}
 
 # The largest length each workload's statement allows (what a contiguous
 # max-length preallocation reserves per sequence).
-WORKLOAD_MAX_LEN = {"qwen2_gqa": 2048, "long_context": 32768, "long_context_mixed": 131072}
+WORKLOAD_MAX_LEN = {"qwen2_gqa": 2048, "long_context": 32768, "long_context_mixed": 131072,
+                    "shared_prefix_fork": 2048, "shared_prefix_prefix": 2048}
 
 
 def memory_report(pa, case, workload: str) -> dict:
@@ -100,7 +140,13 @@ def step_bytes(case, partition: int = 0) -> dict:
     s, hq, hkv, d = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_size
     lens = case.seq_lens.astype(np.int64)
     blocks = int(((lens + case.block_size - 1) // case.block_size).sum())
-    decode = case.kv_bytes() + 2 * s * hq * d * eb + 4 * blocks + 4 * s
+    logical_kv = case.kv_bytes()
+    # Sequences sharing blocks read each shared K/V row once (from DRAM; the
+    # other readers find it in L2): the roofline counts the distinct slots.
+    kv = logical_kv
+    if "unique_slots" in case.meta:
+        kv = case.meta["unique_slots"] * hkv * d * 2 * eb
+    decode = kv + 2 * s * hq * d * eb + 4 * blocks + 4 * s
     partials = 0
     if partition > 0:
         parts = (lens + partition - 1) // partition
@@ -110,7 +156,7 @@ def step_bytes(case, partition: int = 0) -> dict:
     # "step": the workload's bytes, the same whatever partitions a run uses;
     # "decode": what the decode call moves, partials included.
     return {"decode": int(decode + partials), "partials": partials, "write": int(write),
-            "step": int(decode + write)}
+            "step": int(decode + write), "logical_kv": int(logical_kv), "unique_kv": int(kv)}
 
 
 def measured_hbm_peak():
@@ -383,7 +429,10 @@ def run_gpu(args, rank, world, device):
     # in L2 by the previous call), and the same tokens in the unpaged layout
     # (consecutive blocks), L2 evicted, to report what paging costs.
     paging = None
-    if args.paging and world == 1:
+    if args.paging and world == 1 and "unique_slots" in case.meta:
+        paging = {"skipped": "sequences share blocks: a consecutive-block layout would duplicate "
+                             "the shared blocks and read more bytes"}
+    elif args.paging and world == 1:
         n = max(50, args.steps // 4)
         warm = [mk() for _ in range(n)]
         for e0, e1 in warm:
@@ -659,6 +708,8 @@ def main():
                 "decode_kernel": {0: "auto", 1: "cuda cores", 2: "tensor cores"}[args.kernel] +
                                  " -> " + st.kernel_name,
                 "decode_bytes": nbytes["decode"],
+                "kv_bytes_logical": nbytes["logical_kv"],
+                "kv_bytes_unique": nbytes["unique_kv"],
                 "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": st.launches * args.steps,
         "roofline": {
