@@ -124,13 +124,17 @@ pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int num_heads,
       p = 1024;
       while (p > 128 && p > d->block_size && 2 * heads * ((max_seq_len + p - 1) / p) < ctas)
         p >>= 1;
+      // Enough (sequence, KV head) pairs for four items per resident CTA,
+      // and no sequence long enough to leave one CTA a long tail: no split
+      // (no partials, no reduce, no short tail partitions).
+      if (heads >= 4 * ctas && max_seq_len <= 4096) p = 0;
     } else {
       // One CTA per (partition, KV head, sequence): enough CTAs for six per SM.
       p = 512;
       while (p > 64 && p > d->block_size && heads * ((max_seq_len + p - 1) / p) < 6LL * num_sms)
         p >>= 1;
     }
-    if (p < d->block_size) p = d->block_size;
+    if (p > 0 && p < d->block_size) p = d->block_size;
   } else if (p < -1) {
     return PA_ERR_INVALID_ARG;
   } else if (p > 0 && p % d->block_size != 0) {

@@ -53,6 +53,14 @@ cudaError_t launch_reduce_for_head_size(void* out, const float* part_o, const fl
                                         const int32_t* seq_lens, int num_seqs, int num_heads,
                                         int partition_tokens, int max_parts,
                                         cudaStream_t stream) {
+  if (max_parts <= kReduceRowParts) {
+    // Few partitions: a warp per row, eight rows per CTA.
+    const long long rows = (long long)num_seqs * num_heads;
+    void* rargs[] = {&out, &part_o, &part_lse, &seq_lens, &num_seqs, &num_heads,
+                     &partition_tokens, &max_parts};
+    return launch_overlapped((const void*)lse_reduce_rows_kernel<T, D>,
+                             dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, rargs);
+  }
   // Rows of many partitions are shared by several CTAs (32 columns each).
   int cols = max_parts >= 128 ? kReduceMinCols : D;
   dim3 grid((unsigned)num_heads, (unsigned)num_seqs, (unsigned)(D / cols));

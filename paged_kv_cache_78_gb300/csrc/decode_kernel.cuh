@@ -470,6 +470,55 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   }
 }
 
+// Log-sum-exp combination for rows of few partitions (up to
+// kReduceRowParts): one warp per (sequence, query head) row, eight rows per
+// CTA; each lane owns D/32 output columns and walks the row's partitions
+// with four loads in flight.  Same arithmetic as lse_reduce_kernel.
+constexpr int kReduceRowParts = 16;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+    lse_reduce_rows_kernel(void* out_, const float* __restrict__ part_o,
+                           const float* __restrict__ part_lse,
+                           const int32_t* __restrict__ seq_lens, int num_seqs, int num_heads,
+                           int partition_tokens, int max_parts) {
+  using E = ElemTraits<T>;
+  constexpr int kPer = D / 32;  // columns per lane: 2, 4 or 8
+  static_assert(D % 64 == 0, "row reduce columns");
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  grid_dependency_wait();
+  if (row >= (long long)num_seqs * num_heads) return;
+  const int s = (int)(row / num_heads);
+  const int L = seq_lens[s];
+  const int nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
+  if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
+  const float* lse = part_lse + (size_t)row * max_parts;
+  const float* po = part_o + (size_t)row * max_parts * D + lane * kPer;
+  float M = lane < nparts ? lse[lane] : -INFINITY;
+  M = warp_max(M);
+  float w_own = lane < nparts ? fast_exp2(lse[lane] - M) : 0.f;
+  const float wsum = warp_sum(w_own);
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int q = 0; q < nparts; ++q) {
+    const float w = __shfl_sync(0xffffffffu, w_own, q);
+    float v[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+      const float2 t = *reinterpret_cast<const float2*>(po + (size_t)q * D + e);
+      v[e] = t.x;
+      v[e + 1] = t.y;
+    }
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+  }
+  T* out = reinterpret_cast<T*>(out_) + (size_t)row * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) out[e] = E::from_float(acc[e] / wsum);
+}
+
 // Log-sum-exp combination of split-KV partials:
 //   M = max_p lse_p,  w_p = 2^(lse_p - M),  out = sum_p w_p o_p / sum_p w_p.
 // One CTA per (query head, sequence, `cols` output columns): cols = D, or 32

@@ -77,6 +77,8 @@ SHAPES = [
     # many partitions per sequence (the tensor-core kernel numbers only the
     # real items), empty sequences first and last
     (16, 4, 64, 16, [0, 1, 700, 3000, 129, 0], "bf16", (128, 512)),
+    # groups of two (the tensor-core kernel's GP = 2), 20-partition rows
+    (8, 4, 128, 16, [77, 500, 1025, 2560], "bf16", (0, 128, 256)),
 ]
 
 
