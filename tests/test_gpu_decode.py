@@ -188,3 +188,30 @@ def test_decode_trace_records_the_pipeline():
         for w in range(warps):
             t = ev[cta, w, :, 0][tags[cta, w] != 0]
             assert np.all(np.diff(t) >= 0)
+
+
+
+def test_large_batch_without_the_length_cache():
+    # More sequences than the tensor-core kernel keeps lengths of in shared
+    # memory (256): lengths come from global memory, items are numbered sparsely.
+    rng = np.random.default_rng(77)
+    lens = [int(x) for x in rng.integers(0, 300, size=300)]
+    case = workloads.custom(300, 14, 2, 64, 16, lens, "bf16", seed=78)
+    check(case, partitions=(0, 64))
+
+
+def test_automatic_partition_choices():
+    # Tensor-core path: long items, no split when pairs give 4+ items per CTA
+    # and no sequence is long; CUDA-core path: 512 halved toward 64.
+    cache = torch.zeros((2, 4, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert pa.pa_decode_partition_size(cache, 64, 14, 2011, -1) == 1024      # Qwen2 shape
+    assert pa.pa_decode_partition_size(cache, 4 * sms, 14, 2011, -1) == 0    # 8 pairs per SM
+    assert pa.pa_decode_partition_size(cache, 4 * sms, 14, 8192, -1) == 1024  # a long sequence
+    assert pa.pa_decode_partition_size(cache, 64, 14, 1000, -1) == 512       # 128 pairs: split
+    assert pa.pa_decode_partition_size(cache, 64, 14, 300, -1) == 256       # halved to 256
+    assert pa.pa_decode_partition_size(cache, 64, 14, 100, -1) == 0         # one partition
+    c128 = torch.zeros((2, 4, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
+    assert pa.pa_decode_partition_size(c128, 8, 32, 32768, -1) == 1024      # long context
+    mha = torch.zeros((2, 4, 16, 40, 128), dtype=torch.bfloat16, device="cuda")
+    assert pa.pa_decode_partition_size(mha, 32, 40, 2048, -1) == 512        # CUDA cores, G = 1
