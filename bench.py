@@ -299,6 +299,8 @@ class GpuStep:
                                              case.max_seq_len, self.partition)
         self.ws = pa.alloc_workspace(nbytes, device)
         self.launches = 2 + (1 if self.partition > 0 else 0)
+        if int((case.seq_lens > 0).sum()) != case.num_seqs:
+            raise SystemExit("the bench's workloads give every sequence a new token")
         family = pa.pa_decode_select_kernel(self.cache, case.num_seqs, case.num_heads,
                                             self.q.data_ptr(), kernel)
         self.kernel_name = ("paged_decode_tc_kernel" if family == pa.PA_KERNEL_TENSOR
@@ -311,6 +313,14 @@ class GpuStep:
         c = self.case
         self.pa.pa_decode(self.out, self.q, self.cache, self.bt, self.sl, c.scale, c.max_seq_len,
                           self.partition, self.ws, kernel=self.kernel)
+
+    def write_and_decode(self):
+        """The step as one call: the decode writes each sequence's newest
+        token itself (pa_decode_append)."""
+        c = self.case
+        self.pa.pa_decode_append(self.out, self.q, self.cache, self.bt, self.sl, c.scale,
+                                 c.max_seq_len, self.k, self.v, self.partition, self.ws,
+                                 kernel=self.kernel)
 
 
 STEP_INPUTS = ("q", "k", "v", "slots", "bt", "sl")
@@ -385,8 +395,11 @@ def run_gpu(args, rank, world, device):
         g_step, g_write, g_decode = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
                                      torch.cuda.CUDAGraph())
         with torch.cuda.graph(g_step):
-            st.write()
-            st.decode()
+            if args.fused:
+                st.write_and_decode()
+            else:
+                st.write()
+                st.decode()
         with torch.cuda.graph(g_write):
             st.write()
         with torch.cuda.graph(g_decode):
@@ -396,6 +409,8 @@ def run_gpu(args, rank, world, device):
     def step():
         if graphs:
             graphs[0].replay()
+        elif args.fused:
+            st.write_and_decode()
         else:
             st.write()
             st.decode()
@@ -511,8 +526,11 @@ def run_gpu(args, rank, world, device):
 
     def e2e_step():
         arena.copy_(arena_host, non_blocking=True)
-        st.write()
-        st.decode()
+        if args.fused:
+            st.write_and_decode()
+        else:
+            st.write()
+            st.decode()
         out_host.copy_(st.out.view(torch.uint8).view(-1), non_blocking=True)
 
     if not args.e2e:
@@ -649,6 +667,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the CPU baseline (0 = skip)")
     ap.add_argument("--e2e", type=int, default=1, help="also time the step with host buffers")
+    ap.add_argument("--fused", type=int, default=1,
+                    help="1: the step is one pa_decode_append (the decode writes the new tokens); "
+                         "0: pa_reshape_and_cache, then pa_decode")
     ap.add_argument("--paging", type=int, default=1,
                     help="also time the decode warm and on the unpaged (consecutive-block) layout")
     args = ap.parse_args()
@@ -735,13 +756,15 @@ def main():
         "data": "synthetic",
         "config": config_for(case, args.workload, st.partition),
         "run": {"partition_size": st.partition, "cuda_graph": bool(args.graph),
+                "step_calls": "pa_decode_append" if args.fused else
+                              "pa_reshape_and_cache + pa_decode",
                 "decode_kernel": {0: "auto", 1: "cuda cores", 2: "tensor cores"}[args.kernel] +
                                  " -> " + st.kernel_name,
                 "decode_bytes": nbytes["decode"],
                 "kv_bytes_logical": nbytes["logical_kv"],
                 "kv_bytes_unique": nbytes["unique_kv"],
                 "parallelism": "replicas" if world > 1 else "single GPU"},
-        "gpu_launches": st.launches * args.steps,
+        "gpu_launches": (st.launches - (1 if args.fused else 0)) * args.steps,
         "roofline": {
             "kernel": "pa_decode (%s%s)" % (st.kernel_name, " + lse_reduce_kernel" if st.partition else ""),
             "timed": "the decode call alone, %d launches after the timed steps, L2 evicted "

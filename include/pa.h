@@ -191,6 +191,28 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
                        int32_t max_seq_len, int32_t partition_size, void* workspace,
                        size_t workspace_bytes, int32_t kernel, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * pa_decode_ex with the step's cache write fused in: each sequence's newest
+ * token (position seq_lens[s] - 1, the token the decode step appends) has
+ * its keys and values in key_new / value_new, device, cache dtype,
+ * [num_seqs][num_kv_heads][head_size], 16-byte aligned.  Before reading that
+ * token, the decode writes it into the slot its block table gives
+ * (block_tables[s][(L-1) / block_size] * block_size + (L-1) % block_size),
+ * exactly what pa_reshape_and_cache with that slot mapping writes; the
+ * write and the read are one launch instead of two (the pages' decode step
+ * stores the new token's KV in its block, then attends:
+ * studying-code.tistory.com/16, section "디코딩 과정").  Copy-on-write copies
+ * (pa_copy_blocks) must run before.  A sequence of length 0 writes nothing;
+ * a block id outside the pool skips the write and records
+ * PA_DEVERR_BLOCK_ID.  Other arguments and results as pa_decode_ex.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_append(void* out, const void* query, void* cache, const pa_cache_desc* desc,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                           float scale, int32_t max_seq_len, int32_t partition_size,
+                           const void* key_new, const void* value_new, void* workspace,
+                           size_t workspace_bytes, int32_t kernel, void* stream);
+
 /* The kernel family pa_decode_ex(..., kernel, ...) runs for a cache `desc`,
  * num_seqs sequences of num_heads query heads and a query buffer at `query`
  * (its address only decides the 16-byte alignment the tensor-core kernel

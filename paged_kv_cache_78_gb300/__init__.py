@@ -48,7 +48,7 @@ EXPORTS = (
     "pa_version", "pa_set_decode_trace", "pa_pool_add_seq_tokens", "pa_pool_append_token_id",
     "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache", "pa_pool_usage",
     "pa_swap_blocks", "pa_pool_set_cpu_blocks", "pa_pool_swap_out", "pa_pool_swap_in",
-    "pa_pool_is_swapped", "pa_pool_num_free_cpu",
+    "pa_pool_is_swapped", "pa_pool_num_free_cpu", "pa_decode_append",
 )
 
 
@@ -83,6 +83,8 @@ def _load() -> ctypes.CDLL:
         "pa_decode": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, vp],
         "pa_decode_ex": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, sz, i32, vp],
         "pa_decode_no_alloc": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp],
+        "pa_decode_append": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, i32, vp, vp, vp,
+                             sz, i32, vp],
         "pa_decode_partition_size": [desc, i32, i32, i32, i32, p_i32],
         "pa_decode_select_kernel": [desc, i32, i32, vp, i32, p_i32],
         "pa_decode_workspace_size": [desc, i32, i32, i32, i32, p_sz],
@@ -307,6 +309,37 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
                             block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens", torch.int32), s,
                             hq, float(scale), int(max_seq_len), int(partition_size), ws_ptr,
                             ws_bytes, int(kernel), _stream(stream)), "pa_decode")
+
+
+def pa_decode_append(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
+                     block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     max_seq_len: int, key_new: torch.Tensor, value_new: torch.Tensor,
+                     partition_size: int = -1, workspace: torch.Tensor | None = None,
+                     stream=None, kernel: int = PA_KERNEL_AUTO) -> None:
+    """pa_decode that first writes each sequence's newest token (position
+    seq_lens[s] - 1; key_new / value_new [num_seqs, num_kv_heads, head_size])
+    into its cache slot."""
+    desc = cache_desc(cache)
+    s, hq, d = query.shape
+    if out.shape != query.shape or d != desc.head_size:
+        raise ValueError("query/out must be [num_seqs, num_heads, head_size]")
+    for name, t in (("query", query), ("out", out), ("key_new", key_new), ("value_new", value_new)):
+        if t.dtype != cache.dtype:
+            raise TypeError("%s dtype must match the cache" % name)
+    if key_new.shape != (s, desc.num_kv_heads, d) or value_new.shape != key_new.shape:
+        raise ValueError("key_new/value_new must be [num_seqs, num_kv_heads, head_size]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != s or seq_lens.shape != (s,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks], seq_lens [num_seqs]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check(lib.pa_decode_append(_dev_ptr(out, "out"), _dev_ptr(query, "query"),
+                                _dev_ptr(cache, "cache"), ctypes.byref(desc),
+                                _dev_ptr(block_tables, "block_tables", torch.int32),
+                                block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens", torch.int32),
+                                s, hq, float(scale), int(max_seq_len), int(partition_size),
+                                _dev_ptr(key_new, "key_new"), _dev_ptr(value_new, "value_new"),
+                                ws_ptr, ws_bytes, int(kernel), _stream(stream)), "pa_decode_append")
 
 
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20

@@ -375,11 +375,14 @@ pa_status pa_decode(void* out, const void* query, const void* cache, const pa_ca
                       workspace_bytes, PA_KERNEL_AUTO, stream);
 }
 
-pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
-                       const int32_t* block_tables, int32_t max_blocks_per_seq,
-                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
-                       int32_t max_seq_len, int32_t partition_size, void* workspace,
-                       size_t workspace_bytes, int32_t kernel, void* stream) {
+// pa_decode_ex, with the step's newest tokens written into the cache first
+// when new_k / new_v are given (pa_decode_append).
+static pa_status decode_impl(void* out, const void* query, const void* cache,
+                             const pa_cache_desc* desc, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                             int32_t num_heads, float scale, int32_t max_seq_len,
+                             int32_t partition_size, void* workspace, size_t workspace_bytes,
+                             int32_t kernel, const void* new_k, const void* new_v, void* stream) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || num_heads < 1 || max_seq_len < 0 ||
@@ -563,6 +566,9 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
   }
 
   prm.out = out;
+  prm.cache_w = static_cast<uint8_t*>(const_cast<void*>(cache));
+  prm.new_k = new_k;
+  prm.new_v = new_v;
   prm.query = query;
   prm.block_tables = block_tables;
   prm.seq_lens = seq_lens;
@@ -602,6 +608,29 @@ pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+pa_status pa_decode_ex(void* out, const void* query, const void* cache, const pa_cache_desc* desc,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, float scale,
+                       int32_t max_seq_len, int32_t partition_size, void* workspace,
+                       size_t workspace_bytes, int32_t kernel, void* stream) {
+  return decode_impl(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                     num_heads, scale, max_seq_len, partition_size, workspace, workspace_bytes,
+                     kernel, nullptr, nullptr, stream);
+}
+
+pa_status pa_decode_append(void* out, const void* query, void* cache, const pa_cache_desc* desc,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                           float scale, int32_t max_seq_len, int32_t partition_size,
+                           const void* key_new, const void* value_new, void* workspace,
+                           size_t workspace_bytes, int32_t kernel, void* stream) {
+  if (num_seqs > 0 && (!key_new || !value_new || !aligned(key_new, 16) || !aligned(value_new, 16)))
+    return PA_ERR_INVALID_ARG;
+  return decode_impl(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                     num_heads, scale, max_seq_len, partition_size, workspace, workspace_bytes,
+                     kernel, key_new, value_new, stream);
 }
 
 }  // extern "C"

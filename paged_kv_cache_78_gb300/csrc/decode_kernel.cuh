@@ -56,6 +56,9 @@ struct DecodeParams {
   int total_items;              // tensor-core kernel: num_seqs * num_kv_heads * max_parts
   int dense_items;              // tensor-core kernel: number only the real work items
   int num_seqs;
+  uint8_t* cache_w;             // the pool, for the fused cache write (pa_decode_append)
+  const void* new_k;            // [S][Hkv][D] newest token's keys, or null (no fused write)
+  const void* new_v;            // [S][Hkv][D] newest token's values
   unsigned long long* trace;    // tensor-core kernel timeline, or null
   int trace_per_role;
   size_t trace_bytes;
@@ -227,6 +230,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       const int st_tok = tok0 + k * kStageTokens;
       const int st_n = min(kStageTokens, tok1 - st_tok);
       const int nbox = (st_n + R - 1) >> log2R;
+      if (p.new_k != nullptr && tok1 == L && k == n_stages - 1)  // fused write of the newest token
+        write_new_token(p.cache_w, p.new_k, p.new_v, table, s, h, L - 1, p.num_kv_heads,
+                        kRowBytes / 16, BS, l2bs, p.num_blocks, p.err, lane);
       if (lane == 0) mbar_arrive_expect_tx(full0 + 8u * slot, (uint32_t)nbox * stage_tx);
       __syncwarp();
       const uint32_t kdst = sbase + (uint32_t)slot * (uint32_t)p.stage_bytes;

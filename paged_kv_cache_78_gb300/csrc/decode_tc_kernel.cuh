@@ -378,6 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Lane 0 classifies the item; the warp follows its decision.
       TcItem it{0, 0, 0, 0, 0, 0, 0, kItemEnd};
       bool skip = false;
+      int wnew = 0;  // this item holds the sequence's newest token and writes it (fused write)
       if (lane == 0 && dense && idx < total) {
         // The sequence whose items contain idx: the last s with pre[s] <= idx.
         int lo = 0, hi = p.num_seqs - 1;
@@ -399,6 +400,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           it.tok1 = P > 0 ? min(L, it.tok0 + P) : L;
           it.nstages = (it.tok1 - it.tok0 + kTcTokens - 1) / kTcTokens;
           it.final_out = nparts == 1;
+          wnew = p.new_k != nullptr && it.tok1 == L;
         }
       } else if (lane == 0 && !dense && idx < total) {
         it.part = (int)(idx / (unsigned)sh);
@@ -422,9 +424,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           it.tok1 = P > 0 ? min(L, it.tok0 + P) : L;
           it.nstages = (it.tok1 - it.tok0 + kTcTokens - 1) / kTcTokens;
           it.final_out = nparts == 1;
+          wnew = p.new_k != nullptr && it.tok1 == L;
         }
       }
       if (lane == 0) tc_trace(p, 0, ntr, 10, idx);
+      wnew = __shfl_sync(0xffffffffu, wnew, 0);
       skip = __shfl_sync(0xffffffffu, skip, 0);
       if (skip) {
         if (lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
@@ -523,6 +527,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int st_n = min(kTcTokens, it.tok1 - st_tok);
         const int nbox = (st_n + R - 1) >> log2R;
         const int lb0 = st_tok >> l2bs;
+        if (wnew && k == it.nstages - 1)  // the newest token lands in this stage: write it first
+          write_new_token(p.cache_w, p.new_k, p.new_v, table, it.s, it.h, it.tok1 - 1,
+                          p.num_kv_heads, D * 2 / 16, BS, l2bs, p.num_blocks, p.err, lane);
         while (lb0 >= win + 32) {
           cur = nxt;
           win += 32;

@@ -161,6 +161,43 @@ __device__ __forceinline__ void stg_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// ---- the fused cache write ----------------------------------------------------
+
+// Order this thread's generic-proxy global writes before later async-proxy
+// (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Write the newest token (position `pos` of sequence s) of KV head h into
+// its cache slot, keys and values, one 16-byte chunk per lane (rows of
+// `chunks` chunks), then make the writes visible to TMA reads by the warp.
+// The slot's block comes from the sequence's table row; an id outside the
+// pool skips the write and records PA_DEVERR_BLOCK_ID.  Whole warp.
+__device__ __forceinline__ void write_new_token(uint8_t* cache, const void* new_k,
+                                                const void* new_v, const int32_t* table_row,
+                                                int s, int h, int pos, int num_kv_heads,
+                                                int chunks, int block_size, int log2_block_size,
+                                                int num_blocks, unsigned int* err, int lane) {
+  const int id = __ldg(table_row + (pos >> log2_block_size));
+  const bool ok = id >= 0 && id < num_blocks;
+  if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+  const size_t row_bytes = (size_t)num_kv_heads * chunks * 16;
+  for (int i = lane; ok && i < 2 * chunks; i += 32) {
+    const int kv = i >= chunks;
+    const int c = i - kv * chunks;
+    const uint4* src = reinterpret_cast<const uint4*>(kv ? new_v : new_k) +
+                       ((size_t)s * num_kv_heads + h) * chunks + c;
+    uint8_t* dst = cache + (size_t)kv * num_blocks * block_size * row_bytes +
+                   ((size_t)id * block_size + (pos & (block_size - 1))) * row_bytes +
+                   (size_t)h * chunks * 16 + (size_t)c * 16;
+    stg_v4(dst, ldg_nc_v4(src));
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+  fence_proxy_async_global();
+}
+
 // ---- arithmetic -------------------------------------------------------------
 
 // 2^x on the MUFU unit (x = -inf gives +0).

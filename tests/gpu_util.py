@@ -77,6 +77,13 @@ class DeviceCase:
                                              torch.from_numpy(pos)).to(device)
         self.step_keys = to_device(case.keys[rows], device)
         self.step_values = to_device(case.values[rows], device)
+        # the same tokens as one row per sequence (zeros where a sequence is empty)
+        new_k = np.zeros((case.num_seqs,) + case.keys.shape[1:], dtype=case.keys.dtype)
+        new_v = np.zeros_like(new_k)
+        new_k[seqs] = case.keys[rows]
+        new_v[seqs] = case.values[rows]
+        self.new_keys = to_device(new_k, device)
+        self.new_values = to_device(new_v, device)
 
     def step(self, partition_size=-1, workspace=None, kernel=pa.PA_KERNEL_AUTO):
         c = self.case
@@ -87,6 +94,19 @@ class DeviceCase:
             workspace = pa.alloc_workspace(nbytes, self.device)
         pa.pa_decode(self.out, self.query, self.cache, self.block_tables, self.seq_lens,
                      c.scale, c.max_seq_len, partition_size, workspace, kernel=kernel)
+        return self.out
+
+
+    def step_fused(self, partition_size=-1, workspace=None, kernel=pa.PA_KERNEL_AUTO):
+        """The same step with the cache write fused into the decode."""
+        c = self.case
+        if workspace is None:
+            nbytes = pa.pa_decode_workspace_size(self.cache, c.num_seqs, c.num_heads,
+                                                 c.max_seq_len, partition_size)
+            workspace = pa.alloc_workspace(nbytes, self.device)
+        pa.pa_decode_append(self.out, self.query, self.cache, self.block_tables, self.seq_lens,
+                            c.scale, c.max_seq_len, self.new_keys, self.new_values,
+                            partition_size, workspace, kernel=kernel)
         return self.out
 
 

@@ -215,3 +215,34 @@ def test_automatic_partition_choices():
     assert pa.pa_decode_partition_size(c128, 8, 32, 32768, -1) == 1024      # long context
     mha = torch.zeros((2, 4, 16, 40, 128), dtype=torch.bfloat16, device="cuda")
     assert pa.pa_decode_partition_size(mha, 32, 40, 2048, -1) == 512        # CUDA cores, G = 1
+
+
+
+FUSED_SHAPES = [
+    (14, 2, 64, 16, [1, 15, 16, 17, 33, 255, 700, 0], "bf16", (0, 64)),
+    (32, 8, 128, 16, [5, 100, 511, 512, 513, 1500], "bf16", (0, 512)),
+    (4, 4, 128, 8, [0, 1, 31, 32, 33, 129], "bf16", (0, 32)),
+    (32, 8, 128, 16, [7, 300, 1029], "fp32", (0, 256)),
+    (6, 2, 64, 1, [1, 2, 45, 90], "bf16", (0, 8)),
+    (16, 16, 128, 256, [100, 256, 700], "bf16", (0, 512)),
+    (16, 4, 64, 16, [0, 1, 700, 3000, 129, 0], "bf16", (128, 512)),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lens,dtype,parts", FUSED_SHAPES,
+                         ids=["hq%d_hkv%d_d%d_bs%d_%s" % (s[0], s[1], s[2], s[3], s[5])
+                              for s in FUSED_SHAPES])
+def test_decode_with_fused_cache_write(hq, hkv, d, bs, lens, dtype, parts):
+    # pa_decode_append writes each sequence's newest token itself: the cache
+    # ends bit-identical to the separate write, the output matches the oracle.
+    case = workloads.custom(len(lens), hq, hkv, d, bs, lens, dtype,
+                            seed=hq * 100 + d + bs + 7, cache_fill="garbage")
+    ref, cache_ref = oracle_reference(case)
+    for kernel in kernels_for(case):
+        for p in parts:
+            dc = DeviceCase(case)
+            out = dc.step_fused(p, kernel=kernel)
+            torch.cuda.synchronize()
+            assert pa.pa_get_device_error() == 0
+            assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
+            assert_close(to_f64(out), ref, case.dtype, "fused kernel=%d partition=%s" % (kernel, p))
