@@ -131,11 +131,28 @@ def memory_report(pa, case, workload: str) -> dict:
             "contiguous_waste": round(1.0 - used / (len(lens) * max_len), 5)}
 
 
-def step_bytes(case, partition: int = 0) -> dict:
+BALANCED = -2  # the library's PA_PARTITION_BALANCED
+
+
+def balanced_pieces(case, ranges: int) -> np.ndarray:
+    """Pieces of each (sequence, KV head) pair under the balanced split: the
+    pairs' 128-token stages laid end to end, cut every ceil(total / ranges)
+    stages."""
+    n = (case.seq_lens.astype(np.int64) + 127) // 128
+    per_pair = np.repeat(n, case.num_kv_heads)
+    total = int(per_pair.sum())
+    q = max(1, -(-total // ranges))
+    start = np.concatenate([[0], np.cumsum(per_pair)[:-1]])
+    pieces = np.where(per_pair > 0, (start + per_pair - 1) // q - start // q + 1, 0)
+    return pieces
+
+
+def step_bytes(case, partition: int = 0, ranges: int = 0) -> dict:
     """Algorithmic bytes of one step: what the operations must read and write
     once.  With split-KV partitions, each sequence of more than one partition
     also writes and reads its fp32 partials (head_size values and a log-sum-exp
-    per query head and partition)."""
+    per query head and partition); the balanced split (over `ranges` stage
+    ranges) writes and reads those of every pair cut into several pieces."""
     eb = workloads.elem_bytes(case.dtype)
     s, hq, hkv, d = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_size
     lens = case.seq_lens.astype(np.int64)
@@ -151,6 +168,9 @@ def step_bytes(case, partition: int = 0) -> dict:
     if partition > 0:
         parts = (lens + partition - 1) // partition
         partials = int(parts[parts > 1].sum()) * hq * (d + 1) * 4 * 2
+    elif partition == BALANCED:
+        pieces = balanced_pieces(case, ranges)
+        partials = int(pieces[pieces > 1].sum()) * (hq // hkv) * (d + 1) * 4 * 2
     t = int((lens > 0).sum())  # one new token per sequence
     write = t * hkv * d * eb * 2 * 2 + 8 * t  # read new K/V, write them, read slots
     # "step": the workload's bytes, the same whatever partitions a run uses;
@@ -298,7 +318,8 @@ class GpuStep:
         nbytes = pa.pa_decode_workspace_size(self.cache, case.num_seqs, case.num_heads,
                                              case.max_seq_len, self.partition)
         self.ws = pa.alloc_workspace(nbytes, device)
-        self.launches = 2 + (1 if self.partition > 0 else 0)
+        split = self.partition > 0 or (self.partition == BALANCED and case.max_seq_len > 128)
+        self.launches = 2 + (1 if split else 0)
         if int((case.seq_lens > 0).sum()) != case.num_seqs:
             raise SystemExit("the bench's workloads give every sequence a new token")
         family = pa.pa_decode_select_kernel(self.cache, case.num_seqs, case.num_heads,
@@ -369,7 +390,8 @@ def run_gpu(args, rank, world, device):
     partition = args.partition if args.partition != -1 else WORKLOAD_PARTITION.get(args.workload, -1)
     st = GpuStep(torch, pa, case, device, partition, args.kernel)
     arena, arena_host = pack_step_inputs(torch, st, device)
-    nbytes = step_bytes(case, st.partition)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    nbytes = step_bytes(case, st.partition, ranges=sms * (2 if case.head_size == 64 else 1))
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -646,7 +668,7 @@ def config_for(case, name, partition=0):
             "seq_len_min": int(lens.min()), "seq_len_max": int(lens.max()),
             "seq_len_mean": round(float(lens.mean()), 1),
             "new_tokens_per_step": int((lens > 0).sum()),
-            "bytes_per_step": step_bytes(case, partition)["step"],
+            "bytes_per_step": step_bytes(case)["step"],
             "l2": "flushed before every timed step (256 MB write, then 256 MB read)"}
 
 

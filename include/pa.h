@@ -61,6 +61,9 @@ typedef enum pa_dtype { PA_BF16 = 0, PA_FP32 = 1 } pa_dtype;
 #define PA_DEVERR_SEQ_LEN 0x4u     /* decode: seq_len > max_seq_len or > table capacity */
 #define PA_DEVERR_TIMEOUT 0x8u     /* a pipeline wait exceeded its limit (about 2 s) */
 
+/* partition_size of pa_decode: the stage-balanced split (see pa_decode). */
+#define PA_PARTITION_BALANCED (-2)
+
 /* Geometry of one layer's cache. */
 typedef struct pa_cache_desc {
   int32_t num_blocks;    /* physical blocks in the pool, >= 1 */
@@ -152,6 +155,17 @@ pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const v
  *                partial (max, sum, weighted values) in workspace, then
  *                combined by a log-sum-exp reduce kernel.  -1: the library
  *                picks (pa_decode_partition_size reports the choice).
+ *                PA_PARTITION_BALANCED (-2): the tensor-core kernel's
+ *                persistent CTAs get equal shares of the batch's work.  The
+ *                128-token stages of every (sequence, KV head) pair are laid
+ *                end to end and cut into one range of ceil(stages / ranges)
+ *                stages per resident CTA; a pair cut by range ends becomes
+ *                several partials, combined as above.  It applies to the
+ *                tensor-core kernel and batches of up to 256 sequences; for
+ *                other shapes -2 is treated as -1.  If the CUDA-core kernel
+ *                runs the call instead (a query that is not 16-byte aligned,
+ *                or PA_KERNEL_SIMT), it splits into equal partitions that fit
+ *                the same workspace.
  *   workspace    device scratch of at least pa_decode_workspace_size() bytes,
  *                256-byte aligned.  Its first 256 bytes hold the tensor-core
  *                kernel's work counter: they must be zero when the workspace
@@ -223,14 +237,19 @@ pa_status pa_decode_append(void* out, const void* query, void* cache, const pa_c
 pa_status pa_decode_select_kernel(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_heads,
                                   const void* query, int32_t kernel, int32_t* selected);
 
-/* The partition size pa_decode uses for these arguments (0 = no split). */
+/* The partition size pa_decode uses for these arguments (0 = no split,
+ * PA_PARTITION_BALANCED for the balanced split). */
 pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t num_heads, int32_t max_seq_len,
                                    int32_t partition_size, int32_t* resolved);
 
 /* Workspace bytes pa_decode needs for these arguments: a 256-byte header,
  * plus num_seqs * num_heads * max_partitions * (head_size + 1) * 4 (each part
- * rounded up to 256) when it splits. */
+ * rounded up to 256) when it splits.  The balanced split adds
+ * num_seqs * num_kv_heads * 4 bytes (rounded up to 256) of piece counts;
+ * its max_partitions is min(ceil(max_seq_len / 128),
+ * ceil(ranges / num_kv_heads) + 1), where ranges is the number of SMs times
+ * two for head size 64, times one for 128. */
 pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t num_heads, int32_t max_seq_len,
                                    int32_t partition_size, size_t* bytes);
@@ -436,7 +455,8 @@ const char* pa_status_string(pa_status status);
  * (stage).  Softmax warp 2: 14 item taken (item number), 15 scores ready
  * (stage), 5 scores read (stage), 6 P written (stage), 16 stage's P.V added
  * (stage), 7 item output written (item number); warps 3..5: 19 P written
- * (warp << 16 | stage).  Entries beyond a warp's events are left as they
+ * (warp << 16 | stage), 22 item output written (warp << 16 | item number);
+ * warps 2..5: 21 item entry read (warp << 16 | item number).  Entries beyond a warp's events are left as they
  * were.  A launch whose grid needs more than `bytes` records nothing.  NULL
  * turns tracing off (the default).  Host-side setting shared by all threads
  * of the process. */

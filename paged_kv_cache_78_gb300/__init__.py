@@ -36,6 +36,7 @@ PA_DEVERR_SLOT = 0x1
 PA_DEVERR_BLOCK_ID = 0x2
 PA_DEVERR_SEQ_LEN = 0x4
 PA_DEVERR_TIMEOUT = 0x8
+PA_PARTITION_BALANCED = -2
 
 # Every function include/pa.h declares.
 EXPORTS = (

@@ -96,19 +96,51 @@ pa_status check_desc(const pa_cache_desc* d) {
 
 bool head_size_supported(int d) { return d == 64 || d == 128 || d == 256; }
 
-// Partition policy.  An explicit size is checked; -1 picks the largest of
-// 512, 256, 128, 64 tokens (not below the block size) that still gives about
-// three CTAs per SM when sequences average half of max_seq_len.  A size that
-// covers max_seq_len means no split (0).
+// Partition policy.  An explicit size is checked.  -1 on the CUDA-core
+// kernel picks the largest of 512, 256, 128, 64 tokens (not below the block
+// size) that still gives six CTAs per SM; on the tensor-core kernel it picks
+// no split when (sequence, KV head) pairs alone fill the grid, else the
+// balanced split (1024-token partitions and down for batches of more than
+// 256 sequences).  A size that covers max_seq_len means no split (0).
 pa_status select_kernel(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_heads,
                         const void* query, int32_t kernel, int32_t* selected);
 
 // The automatic partition size depends only on the shapes and on the kernel
 // family PA_KERNEL_AUTO picks for a 16-byte aligned query, so the size
 // queries and the decode call always agree.
+// Stage ranges of the balanced split: one per resident CTA of the
+// tensor-core kernel (two per SM for head size 64, one for 128).
+int balanced_ranges(const pa_cache_desc* d, int num_sms) {
+  return num_sms * (d->head_size == 64 ? 2 : 1);
+}
+
+// Partials per row of the balanced split.  A pair of n stages meets at most
+// ceil((n - 1) / Q) + 1 ranges of Q stages; every sequence has num_kv_heads
+// pairs, so n <= Q * ranges / num_kv_heads, and n <= ceil(max_seq_len / 128).
+int balanced_max_parts(const pa_cache_desc* d, int max_seq_len, int num_sms) {
+  const long long by_len = ((long long)max_seq_len + pa::kTcTokens - 1) / pa::kTcTokens;
+  const long long by_ranges =
+      ((long long)balanced_ranges(d, num_sms) + d->num_kv_heads - 1) / d->num_kv_heads + 1;
+  const long long m = by_len < by_ranges ? by_len : by_ranges;
+  return m < 1 ? 1 : (int)m;
+}
+
 pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int num_heads, int max_seq_len,
                             int requested, int num_sms, int* out) {
   int p = requested;
+  if (p == PA_PARTITION_BALANCED) {
+    // The balanced split runs on the tensor-core kernel, for batches whose
+    // lengths it keeps in shared memory; elsewhere the automatic rule.
+    int32_t family = PA_KERNEL_SIMT;
+    if (select_kernel(d, num_seqs, num_heads, reinterpret_cast<const void*>(256), PA_KERNEL_AUTO,
+                      &family) != PA_OK)
+      family = PA_KERNEL_SIMT;
+    if (family == PA_KERNEL_TENSOR && num_seqs <= pa::kTcLensCache) {
+      *out = PA_PARTITION_BALANCED;
+      return PA_OK;
+    }
+    p = -1;
+  }
   if (p == -1) {
     const long long heads = (long long)num_seqs * d->num_kv_heads;
     int32_t family = PA_KERNEL_SIMT;
@@ -128,6 +160,13 @@ pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int num_heads,
       // and no sequence long enough to leave one CTA a long tail: no split
       // (no partials, no reduce, no short tail partitions).
       if (heads >= 4 * ctas && max_seq_len <= 4096) p = 0;
+      // Where that splits, the balanced split instead (batches whose lengths
+      // the kernel keeps in shared memory): every CTA gets the same number of
+      // stages, so no long item leaves a tail.
+      if (p > 0 && p < max_seq_len && num_seqs <= pa::kTcLensCache) {
+        *out = PA_PARTITION_BALANCED;
+        return PA_OK;
+      }
     } else {
       // One CTA per (partition, KV head, sequence): enough CTAs for six per SM.
       p = 512;
@@ -135,7 +174,7 @@ pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int num_heads,
         p >>= 1;
     }
     if (p > 0 && p < d->block_size) p = d->block_size;
-  } else if (p < -1) {
+  } else if (p < PA_PARTITION_BALANCED) {
     return PA_ERR_INVALID_ARG;
   } else if (p > 0 && p % d->block_size != 0) {
     return PA_ERR_INVALID_ARG;
@@ -154,11 +193,14 @@ size_t partial_o_bytes(int num_seqs, int num_heads, int head_size, int max_parts
   return (rows * head_size * 4 + 255) / 256 * 256;
 }
 
-size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_parts) {
+// pairs: (sequence, KV head) pairs whose piece counts follow the partials
+// (balanced split), else 0.
+size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_parts,
+                           size_t pairs = 0) {
   if (max_parts == 0) return kWorkspaceHeader;
   const size_t rows = (size_t)num_seqs * num_heads * max_parts;
   return kWorkspaceHeader + partial_o_bytes(num_seqs, num_heads, head_size, max_parts) +
-         (rows * 4 + 255) / 256 * 256;
+         (rows * 4 + 255) / 256 * 256 + (pairs * 4 + 255) / 256 * 256;
 }
 
 // The kernel family for a decode call (desc already checked).
@@ -332,7 +374,7 @@ pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
       num_heads % desc->num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
   int sms = 0;
-  if (partition_size == -1 && (st = device_state(nullptr, &sms)) != PA_OK) return st;
+  if (partition_size < 0 && (st = device_state(nullptr, &sms)) != PA_OK) return st;
   int p = 0;
   if ((st = resolve_partition(desc, num_seqs, num_heads, max_seq_len, partition_size, sms, &p)) !=
       PA_OK)
@@ -349,6 +391,14 @@ pa_status pa_decode_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
   pa_status st = pa_decode_partition_size(desc, num_seqs, num_heads, max_seq_len,
                                           partition_size, &p);
   if (st != PA_OK) return st;
+  if (p == PA_PARTITION_BALANCED) {
+    int sms = 0;
+    if ((st = device_state(nullptr, &sms)) != PA_OK) return st;
+    *bytes = workspace_bytes_for(num_seqs, num_heads, desc->head_size,
+                                 balanced_max_parts(desc, max_seq_len, sms),
+                                 (size_t)num_seqs * desc->num_kv_heads);
+    return PA_OK;
+  }
   *bytes = workspace_bytes_for(num_seqs, num_heads, desc->head_size,
                                p == 0 ? 0 : (max_seq_len + p - 1) / p);
   return PA_OK;
@@ -411,20 +461,40 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
   if ((st = resolve_partition(desc, num_seqs, num_heads, max_seq_len, partition_size, sms,
                               &part)) != PA_OK)
     return st;
-  const int max_parts = part > 0 ? (max_seq_len + part - 1) / part : 1;
+  bool balanced = part == PA_PARTITION_BALANCED;
+  if (balanced && !use_tc) {
+    // The CUDA-core kernel (a query the tensor-core kernel cannot load, or
+    // an explicit family) splits into equal partitions instead, no more of
+    // them than the balanced split's partials, so its workspace suffices.
+    const int mp = balanced_max_parts(desc, max_seq_len, sms);
+    part = (max_seq_len + mp - 1) / mp;
+    part = (part + BS - 1) / BS * BS;
+    if (part >= max_seq_len) part = 0;
+    balanced = false;
+  }
+  const int max_parts = balanced  ? balanced_max_parts(desc, max_seq_len, sms)
+                        : part > 0 ? (max_seq_len + part - 1) / part
+                                   : 1;
+  const size_t pairs = balanced ? (size_t)num_seqs * desc->num_kv_heads : 0;
   float* part_o = nullptr;
   float* part_lse = nullptr;
+  int32_t* part_counts = nullptr;
   unsigned int* sched = nullptr;
-  if (part > 0 || use_tc) {
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, D, part > 0 ? max_parts : 0);
+  if (part > 0 || balanced || use_tc) {
+    const size_t need =
+        workspace_bytes_for(num_seqs, num_heads, D, part > 0 || balanced ? max_parts : 0, pairs);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
       return PA_ERR_INVALID_ARG;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     sched = reinterpret_cast<unsigned int*>(ws);
-    if (part > 0) {
+    if (part > 0 || balanced) {
+      const size_t o_bytes = partial_o_bytes(num_seqs, num_heads, D, max_parts);
+      const size_t rows = (size_t)num_seqs * num_heads * max_parts;
       part_o = reinterpret_cast<float*>(ws + kWorkspaceHeader);
-      part_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader +
-                                          partial_o_bytes(num_seqs, num_heads, D, max_parts));
+      part_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader + o_bytes);
+      if (balanced)
+        part_counts = reinterpret_cast<int32_t*>(ws + kWorkspaceHeader + o_bytes +
+                                                 (rows * 4 + 255) / 256 * 256);
     }
   }
 
@@ -447,7 +517,12 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     // With many partitions per sequence most (partition, sequence, head)
     // slots of a mixed-length batch are past a sequence's end; the kernel
     // then numbers only the real items (batches it caches in shared memory).
-    prm.dense_items = max_parts > 4 && num_seqs <= pa::kTcLensCache;
+    prm.dense_items = !balanced && max_parts > 4 && num_seqs <= pa::kTcLensCache;
+    if (balanced) {
+      prm.balanced = 1;
+      prm.total_items = balanced_ranges(desc, sms);
+      prm.part_counts = part_counts;
+    }
   } else {
     // 32-token stages, TMA boxes of min(block_size, 32) rows, one box per
     // 128-byte column group, each box at a 1024-byte aligned slot so the
@@ -583,7 +658,7 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
   prm.num_seqs = num_seqs;
   prm.group = group;
   prm.max_blocks_per_seq = max_blocks_per_seq;
-  prm.partition_tokens = part;
+  prm.partition_tokens = balanced ? 0 : part;
   prm.max_parts = max_parts;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
   prm.box_rows = R;
@@ -601,9 +676,9 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     e = pa::launch_decode_f32(D, group, grid, smem, s, map, prm, &supported);
   if (!supported) return PA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (part > 0) {
-    e = pa::launch_lse_reduce(desc->dtype, D, out, part_o, part_lse, seq_lens, num_seqs,
-                              num_heads, part, max_parts, s, &supported);
+  if (part > 0 || (balanced && max_parts > 1)) {
+    e = pa::launch_lse_reduce(desc->dtype, D, out, part_o, part_lse, seq_lens, part_counts, group,
+                              num_seqs, num_heads, balanced ? 0 : part, max_parts, s, &supported);
     if (!supported) return PA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }

@@ -8,7 +8,7 @@ namespace pa {
   cudaError_t launch_decode_##TAG##_d##D(int, dim3, int, cudaStream_t, const CUtensorMap&,   \
                                          const DecodeParams&, bool*);                        \
   cudaError_t launch_reduce_##TAG##_d##D(void*, const float*, const float*, const int32_t*,  \
-                                         int, int, int, int, cudaStream_t);
+                                         const int32_t*, int, int, int, int, int, cudaStream_t);
 PA_DECLARE_UNIT(bf16, 64)
 PA_DECLARE_UNIT(bf16, 128)
 PA_DECLARE_UNIT(bf16, 256)
@@ -40,14 +40,15 @@ cudaError_t launch_decode_f32(int head_size, int group, dim3 grid, int smem_byte
 }
 
 cudaError_t launch_lse_reduce(int dtype, int head_size, void* out, const float* part_o,
-                              const float* part_lse, const int32_t* seq_lens, int num_seqs,
-                              int num_heads, int partition_tokens, int max_parts,
-                              cudaStream_t stream, bool* supported) {
+                              const float* part_lse, const int32_t* seq_lens,
+                              const int32_t* counts, int group, int num_seqs, int num_heads,
+                              int partition_tokens, int max_parts, cudaStream_t stream,
+                              bool* supported) {
   *supported = true;
-#define PA_REDUCE_CASE(TAG, D)                                                            \
-  case D:                                                                                 \
-    return launch_reduce_##TAG##_d##D(out, part_o, part_lse, seq_lens, num_seqs, num_heads, \
-                                      partition_tokens, max_parts, stream);
+#define PA_REDUCE_CASE(TAG, D)                                                                \
+  case D:                                                                                     \
+    return launch_reduce_##TAG##_d##D(out, part_o, part_lse, seq_lens, counts, group, num_seqs, \
+                                      num_heads, partition_tokens, max_parts, stream);
   if (dtype == 0) {
     switch (head_size) { PA_REDUCE_CASE(bf16, 64) PA_REDUCE_CASE(bf16, 128) PA_REDUCE_CASE(bf16, 256) }
   } else {

@@ -50,13 +50,14 @@ cudaError_t launch_decode_for_head_size(int group, dim3 grid, int smem_bytes,
 
 template <typename T, int D>
 cudaError_t launch_reduce_for_head_size(void* out, const float* part_o, const float* part_lse,
-                                        const int32_t* seq_lens, int num_seqs, int num_heads,
+                                        const int32_t* seq_lens, const int32_t* counts,
+                                        int group, int num_seqs, int num_heads,
                                         int partition_tokens, int max_parts,
                                         cudaStream_t stream) {
   if (max_parts <= kReduceRowParts) {
     // Few partitions: a warp per row, eight rows per CTA.
     const long long rows = (long long)num_seqs * num_heads;
-    void* rargs[] = {&out, &part_o, &part_lse, &seq_lens, &num_seqs, &num_heads,
+    void* rargs[] = {&out, &part_o, &part_lse, &seq_lens, &counts, &group, &num_seqs, &num_heads,
                      &partition_tokens, &max_parts};
     return launch_overlapped((const void*)lse_reduce_rows_kernel<T, D>,
                              dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, rargs);
@@ -64,8 +65,8 @@ cudaError_t launch_reduce_for_head_size(void* out, const float* part_o, const fl
   // Rows of many partitions are shared by several CTAs (32 columns each).
   int cols = max_parts >= 128 ? kReduceMinCols : D;
   dim3 grid((unsigned)num_heads, (unsigned)num_seqs, (unsigned)(D / cols));
-  void* args[] = {&out, &part_o, &part_lse, &seq_lens, &num_heads, &partition_tokens, &max_parts,
-                  &cols};
+  void* args[] = {&out,   &part_o,    &part_lse,         &seq_lens,  &counts, &group,
+                  &num_heads, &partition_tokens, &max_parts, &cols};
   return launch_overlapped((const void*)lse_reduce_kernel<T, D>, grid, dim3(kReduceThreads), 0,
                            stream, args);
 }
@@ -82,10 +83,11 @@ cudaError_t launch_reduce_for_head_size(void* out, const float* part_o, const fl
   }                                                                                            \
   cudaError_t launch_reduce_##TAG##_d##D(void* out, const float* part_o,                       \
                                          const float* part_lse, const int32_t* seq_lens,       \
-                                         int num_seqs, int num_heads, int partition_tokens,    \
-                                         int max_parts, cudaStream_t stream) {                 \
-    return launch_reduce_for_head_size<TYPE, D>(out, part_o, part_lse, seq_lens, num_seqs,     \
-                                                num_heads, partition_tokens, max_parts,        \
-                                                stream);                                       \
+                                         const int32_t* counts, int group, int num_seqs,       \
+                                         int num_heads, int partition_tokens, int max_parts,   \
+                                         cudaStream_t stream) {                                \
+    return launch_reduce_for_head_size<TYPE, D>(out, part_o, part_lse, seq_lens, counts,       \
+                                                group, num_seqs, num_heads, partition_tokens,  \
+                                                max_parts, stream);                            \
   }                                                                                            \
   }

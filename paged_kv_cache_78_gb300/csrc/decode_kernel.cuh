@@ -54,7 +54,10 @@ struct DecodeParams {
   unsigned int* err;            // device error word
   unsigned int* sched;          // tensor-core kernel: [0] next work item, [1] CTAs finished
   int total_items;              // tensor-core kernel: num_seqs * num_kv_heads * max_parts
+                                // (balanced split: the number of stage ranges)
   int dense_items;              // tensor-core kernel: number only the real work items
+  int balanced;                 // tensor-core kernel: stage-balanced split (ranges of stages)
+  int32_t* part_counts;         // balanced split: [S][Hkv] pieces of each pair (1 = final rows)
   int num_seqs;
   uint8_t* cache_w;             // the pool, for the fused cache write (pa_decode_append)
   const void* new_k;            // [S][Hkv][D] newest token's keys, or null (no fused write)
@@ -486,8 +489,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
     lse_reduce_rows_kernel(void* out_, const float* __restrict__ part_o,
                            const float* __restrict__ part_lse,
-                           const int32_t* __restrict__ seq_lens, int num_seqs, int num_heads,
-                           int partition_tokens, int max_parts) {
+                           const int32_t* __restrict__ seq_lens,
+                           const int32_t* __restrict__ counts, int group, int num_seqs,
+                           int num_heads, int partition_tokens, int max_parts) {
   using E = ElemTraits<T>;
   constexpr int kPer = D / 32;  // columns per lane: 2, 4 or 8
   static_assert(D % 64 == 0, "row reduce columns");
@@ -495,9 +499,13 @@ __global__ void __launch_bounds__(256)
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   grid_dependency_wait();
   if (row >= (long long)num_seqs * num_heads) return;
-  const int s = (int)(row / num_heads);
-  const int L = seq_lens[s];
-  const int nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
+  int nparts;
+  if (counts != nullptr) {
+    nparts = counts[row / group];  // pieces of the row's (sequence, KV head) pair
+  } else {
+    const int L = seq_lens[row / num_heads];
+    nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
+  }
   if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
   const float* lse = part_lse + (size_t)row * max_parts;
   const float* po = part_o + (size_t)row * max_parts * D + lane * kPer;
@@ -541,7 +549,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads, 4)
     lse_reduce_kernel(void* out_, const float* __restrict__ part_o,
                       const float* __restrict__ part_lse, const int32_t* __restrict__ seq_lens,
-                      int num_heads, int partition_tokens, int max_parts, int cols) {
+                      const int32_t* __restrict__ counts, int group, int num_heads,
+                      int partition_tokens, int max_parts, int cols) {
   using E = ElemTraits<T>;
   static_assert(D % kReduceMinCols == 0, "reduce columns");
   constexpr int kRowF4 = D / 4;  // float4 columns of a partial row
@@ -557,10 +566,15 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
   const int lane = tid & 31;
   const int warp = tid >> 5;
   grid_dependency_wait();
-  const int L = seq_lens[s];
-  const int nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
-  if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
   const size_t row = (size_t)s * num_heads + hq;
+  int nparts;
+  if (counts != nullptr) {
+    nparts = counts[row / group];  // pieces of the row's (sequence, KV head) pair
+  } else {
+    const int L = seq_lens[s];
+    nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
+  }
+  if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
   const float* lse = part_lse + row * max_parts;
   const float4* po = reinterpret_cast<const float4*>(part_o + row * max_parts * D + col0);
 

@@ -13,7 +13,8 @@
 // The 16 columns are the query heads of one KV head (G <= 16; rows past G
 // are masked).  A work item is one (partition, KV head, sequence).  The grid
 // is persistent: each CTA takes items from an atomic counter until they run
-// out, and its six warps stream every item's stages through one pipeline:
+// out (or, in the balanced split, the pieces of its own ranges of stages),
+// and its six warps stream every item's stages through one pipeline:
 //   warp 0      producer: takes the next item, publishes it in a 4-entry ring,
 //               loads the item's 16 query rows by TMA straight into the
 //               swizzled B-operand layout, and streams the item's 128-token
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // counter); the producer loads its block-table window now, overlapping the
   // sequence-length loads below.
   int pf_win = -1, pf_s = -1, pf_cur = 0, pf_nxt = 0;
-  if (warp == 0 && !p.dense_items && (int)blockIdx.x < p.total_items) {
+  if (warp == 0 && !p.dense_items && !p.balanced && (int)blockIdx.x < p.total_items) {
     const int sh = p.num_seqs * p.num_kv_heads;
     const int part = (int)blockIdx.x / sh;
     pf_s = ((int)blockIdx.x - part * sh) / p.num_kv_heads;
@@ -342,9 +343,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // a partition past a sequence's end.  pre[] is a warp scan of the
     // per-sequence item counts.  Otherwise item = (partition, sequence, KV
     // head) over the whole grid, partitions past a sequence's end skipped.
+    //
+    // Balanced split: the stages of every (sequence, KV head) pair, laid end
+    // to end (sequences in order, KV heads fastest), are cut into
+    // p.total_items ranges of Q = ceil(stages / ranges) stages; CTA b takes
+    // ranges b, b + grid, ...  A range covers the end of one pair and the
+    // start of the next ones; each such piece is a work item.  pre[s] then
+    // counts the stages before sequence s, the pieces of a pair are its
+    // partials (numbered by range), and the CTA holding a pair's first piece
+    // records the pair's piece count for the reduce.  Sequences without
+    // stages (length 0, or a length error) are handled after the ranges,
+    // sequence s by CTA s mod grid.
     int* pre = reinterpret_cast<int*>(base + lay.pre_off);
     unsigned int total = (unsigned)p.total_items;
-    const bool dense = p.dense_items && lens_s != nullptr;
+    const bool bal = p.balanced && lens_s != nullptr;
+    const bool dense = (p.dense_items || bal) && lens_s != nullptr;
     if (dense) {
       int carry = 0;
       if (lane == 0) pre[0] = 0;
@@ -354,9 +367,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (sq < p.num_seqs) {
           const int L = lens_s[sq];
           const int np = L <= 0 ? 1 : (P > 0 ? (L + P - 1) / P : 1);
-          if (L > 0 && ((P > 0 && np > p.max_parts) ||
+          if (L > 0 && ((!bal && P > 0 && np > p.max_parts) ||
                         ((L + BS - 1) >> l2bs) > p.max_blocks_per_seq)) {
             if (blockIdx.x == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
+          } else if (bal) {
+            n = L <= 0 ? 0 : ((L + kTcTokens - 1) / kTcTokens) * p.num_kv_heads;
           } else {
             n = np * p.num_kv_heads;
           }
@@ -373,13 +388,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       total = (unsigned)carry;
     }
     unsigned int idx = blockIdx.x;
+    // Balanced split cursor (lane 0): stages [bg, bg_end) of range brange,
+    // then sequence zs (KV head zh) of the zero-stage pass.
+    const int ranges = p.total_items;
+    const int bq = bal ? max(1, (int)((total + (unsigned)ranges - 1) / (unsigned)ranges)) : 1;
+    int brange = (int)blockIdx.x, bg = 0, bg_end = 0, zs = (int)blockIdx.x, zh = 0;
+    if (bal && brange < ranges) {
+      bg = brange * bq;
+      bg_end = min((int)total, bg + bq);
+    }
     while (true) {
       if (flags[0]) break;
       // Lane 0 classifies the item; the warp follows its decision.
       TcItem it{0, 0, 0, 0, 0, 0, 0, kItemEnd};
       bool skip = false;
       int wnew = 0;  // this item holds the sequence's newest token and writes it (fused write)
-      if (lane == 0 && dense && idx < total) {
+      if (lane == 0 && bal) {
+        if (bg < bg_end) {
+          // The sequence whose stages contain bg: the last s with pre[s] <= bg.
+          int lo = 0, hi = p.num_seqs - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= bg) lo = mid; else hi = mid - 1;
+          }
+          const int L = lens_s[lo];
+          const int n = (L + kTcTokens - 1) / kTcTokens;  // stages of each of its pairs
+          const int off = bg - pre[lo];
+          const int h = off / n;
+          const int k0 = off - h * n;
+          const int len = min(n - k0, bg_end - bg);
+          const int pair0 = pre[lo] + h * n;  // the pair's first stage
+          const int first = pair0 / bq;
+          const int npieces = (pair0 + n - 1) / bq - first + 1;
+          it.s = lo;
+          it.h = h;
+          it.part = bg / bq - first;
+          it.tok0 = k0 * kTcTokens;
+          it.tok1 = min(L, (k0 + len) * kTcTokens);
+          it.nstages = len;
+          it.final_out = npieces == 1;
+          it.kind = kItemAttend;
+          if (it.part == 0) {
+            p.part_counts[lo * p.num_kv_heads + h] = npieces <= p.max_parts ? npieces : 0;
+            if (npieces > p.max_parts) record_error(p.err, PA_DEVERR_SEQ_LEN);
+          }
+          skip = npieces > p.max_parts;
+          wnew = p.new_k != nullptr && it.tok1 == L;
+          bg += len;
+          if (bg >= bg_end) {
+            brange += (int)gridDim.x;
+            if (brange < ranges) {
+              bg = brange * bq;
+              bg_end = min((int)total, bg + bq);
+            }
+          }
+        } else if (zs < p.num_seqs) {
+          if (pre[zs + 1] == pre[zs]) {
+            // No stages: zero rows for length 0 (a length error leaves its
+            // rows undefined); no partials either way.
+            p.part_counts[zs * p.num_kv_heads + zh] = 0;
+            it.s = zs;
+            it.h = zh;
+            it.kind = kItemZero;
+            skip = lens_s[zs] > 0;
+            if (++zh == p.num_kv_heads) {
+              zh = 0;
+              zs += (int)gridDim.x;
+            }
+          } else {
+            skip = true;
+            zs += (int)gridDim.x;
+          }
+        }
+      } else if (lane == 0 && dense && idx < total) {
         // The sequence whose items contain idx: the last s with pre[s] <= idx.
         int lo = 0, hi = p.num_seqs - 1;
         while (lo < hi) {
@@ -427,11 +508,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wnew = p.new_k != nullptr && it.tok1 == L;
         }
       }
-      if (lane == 0) tc_trace(p, 0, ntr, 10, idx);
+      if (lane == 0) tc_trace(p, 0, ntr, 10, bal ? (uint32_t)bg : idx);
       wnew = __shfl_sync(0xffffffffu, wnew, 0);
       skip = __shfl_sync(0xffffffffu, skip, 0);
       if (skip) {
-        if (lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
+        if (lane == 0 && !bal) idx = gridDim.x + atomicAdd(p.sched, 1u);
         continue;
       }
       it.s = __shfl_sync(0xffffffffu, it.s, 0);
@@ -471,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) tc_trace(p, 0, ntr, 8, (uint32_t)ii);
         break;
       }
-      if (lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
+      if (lane == 0 && !bal) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
       if (it.kind != kItemAttend) continue;
 
       // Query rows h*G .. h*G+15 of sequence s (rows past G are masked).
@@ -735,6 +816,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       it.nstages = ring[j].nstages;
       it.final_out = ring[j].final_out;
       it.kind = ring[j].kind;
+      if (lane == 0) tc_trace(p, warp, ntr, 21, (uint32_t)((warp << 16) | ii));
       ok = softmax_group_all(w && ok && !flags[0]);  // every thread has read the entry
       if (!ok) break;
       if (tid == 64) {
@@ -868,24 +950,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) red2[q4 * kTcHeads + g] = s_;
       }
       if (!(ok = softmax_group_all(ok && !flags[0]))) break;
-      if (row < D) {
-        const int d = row;
+      {
+        // One warp runs this once per item, so its instruction count is its
+        // latency: per-head work (the sum over the four quarters, the
+        // reciprocal, the log-sum-exp) is done by lane g for head g, in
+        // parallel, and broadcast; lane i then writes column d of its heads.
+        // For D = 128 each warp holds 32 columns of every head.  For D = 64
+        // rows 64..127 of O^T repeat rows 0..63, so warps 2, 3 hold the same
+        // columns as warps 4, 5, and the heads are split between the pairs.
+        const int d = row & (D - 1);
+        const int g_lo = D == 64 ? (q4 >> 1) * ((G + 1) >> 1) : 0;
+        const int g_hi = D == 64 ? min(G, g_lo + ((G + 1) >> 1)) : G;
+        float lsum_l = 1.f, m_l = 0.f;
+        if (lane < GP) {
+          lsum_l = red2[lane] + red2[kTcHeads + lane] + red2[2 * kTcHeads + lane] +
+                   red2[3 * kTcHeads + lane];
+#pragma unroll
+          for (int g = 0; g < GP; ++g)
+            if (lane == g) m_l = m_run[g];
+        }
+        const float inv_l = 1.f / lsum_l;
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          if (g >= G) continue;
-          const float lsum = red2[g] + red2[kTcHeads + g] + red2[2 * kTcHeads + g] +
-                             red2[3 * kTcHeads + g];
-          const float val = o_acc[g] / lsum;
-          if (it.final_out) {
+          const float val = o_acc[g] * __shfl_sync(0xffffffffu, inv_l, g);
+          if (g < g_lo || g >= g_hi) continue;
+          if (it.final_out)
             reinterpret_cast<__nv_bfloat16*>(p.out)[(row0 + g) * D + d] = __float2bfloat16_rn(val);
-          } else {
-            const size_t prow = (row0 + g) * (size_t)p.max_parts + it.part;
-            p.part_o[prow * D + d] = val;
-            if (d == 0) p.part_lse[prow] = m_run[g] + log2f(lsum);
-          }
+          else
+            p.part_o[((row0 + g) * (size_t)p.max_parts + it.part) * D + d] = val;
         }
+        if (!it.final_out && q4 == 0 && lane < G)
+          p.part_lse[(row0 + lane) * (size_t)p.max_parts + it.part] = m_l + log2f(lsum_l);
       }
       if (tid == 64) tc_trace(p, 2, ntr, 7, (uint32_t)ii);
+      else if (lane == 0) tc_trace(p, warp, ntr, 22, (uint32_t)((warp << 16) | ii));
     }
     if (!ok) flags[0] = 1;
   }

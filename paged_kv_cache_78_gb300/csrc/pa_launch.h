@@ -52,9 +52,13 @@ cudaError_t launch_decode_tc(int head_size, int num_sms, int smem_bytes, cudaStr
                              const CUtensorMap& kv_map, const CUtensorMap& q_map,
                              const DecodeParams& params, bool* supported);
 
+// Log-sum-exp reduce of split-KV partials.  A row's partial count comes from
+// counts[row / group] when counts is given (balanced split), else from its
+// sequence length and partition_tokens.
 cudaError_t launch_lse_reduce(int dtype, int head_size, void* out, const float* part_o,
-                              const float* part_lse, const int32_t* seq_lens, int num_seqs,
-                              int num_heads, int partition_tokens, int max_parts,
-                              cudaStream_t stream, bool* supported);
+                              const float* part_lse, const int32_t* seq_lens,
+                              const int32_t* counts, int group, int num_seqs, int num_heads,
+                              int partition_tokens, int max_parts, cudaStream_t stream,
+                              bool* supported);
 
 }  // namespace pa

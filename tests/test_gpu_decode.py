@@ -33,9 +33,11 @@ def kernels_for(case):
 
 
 def check(case, partitions=(0, -1)):
+    # Every case also runs the balanced split (on the CUDA-core kernel it
+    # becomes equal partitions sized to the same workspace).
     ref, cache_ref = oracle_reference(case)
     for kernel in kernels_for(case):
-        for p in partitions:
+        for p in tuple(partitions) + (pa.PA_PARTITION_BALANCED,):
             dc = DeviceCase(case)
             out = dc.step(p, kernel=kernel)
             torch.cuda.synchronize()
@@ -201,20 +203,94 @@ def test_large_batch_without_the_length_cache():
 
 
 def test_automatic_partition_choices():
-    # Tensor-core path: long items, no split when pairs give 4+ items per CTA
-    # and no sequence is long; CUDA-core path: 512 halved toward 64.
+    # Tensor-core path: no split when pairs give 4+ items per CTA and no
+    # sequence is long, else the balanced split (long items beyond 256
+    # sequences); CUDA-core path: 512 halved toward 64.
     cache = torch.zeros((2, 4, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert pa.pa_decode_partition_size(cache, 64, 14, 2011, -1) == 1024      # Qwen2 shape
+    B = pa.PA_PARTITION_BALANCED
+    assert pa.pa_decode_partition_size(cache, 64, 14, 2011, -1) == B        # Qwen2 shape
     assert pa.pa_decode_partition_size(cache, 4 * sms, 14, 2011, -1) == 0    # 8 pairs per SM
-    assert pa.pa_decode_partition_size(cache, 4 * sms, 14, 8192, -1) == 1024  # a long sequence
-    assert pa.pa_decode_partition_size(cache, 64, 14, 1000, -1) == 512       # 128 pairs: split
-    assert pa.pa_decode_partition_size(cache, 64, 14, 300, -1) == 256       # halved to 256
-    assert pa.pa_decode_partition_size(cache, 64, 14, 100, -1) == 0         # one partition
+    assert pa.pa_decode_partition_size(cache, 4 * sms, 14, 8192, -1) == 1024  # > 256 sequences
+    assert pa.pa_decode_partition_size(cache, 64, 14, 1000, -1) == B         # 128 pairs: split
+    assert pa.pa_decode_partition_size(cache, 64, 14, 100, -1) == 0          # one partition
     c128 = torch.zeros((2, 4, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
-    assert pa.pa_decode_partition_size(c128, 8, 32, 32768, -1) == 1024      # long context
+    assert pa.pa_decode_partition_size(c128, 8, 32, 32768, -1) == B         # long context
     mha = torch.zeros((2, 4, 16, 40, 128), dtype=torch.bfloat16, device="cuda")
     assert pa.pa_decode_partition_size(mha, 32, 40, 2048, -1) == 512        # CUDA cores, G = 1
+
+
+def test_balanced_split_applies_to_the_tensor_core_kernel_only():
+    B = pa.PA_PARTITION_BALANCED
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cache = torch.zeros((2, 4, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    assert pa.pa_decode_partition_size(cache, 64, 14, 2011, B) == B
+    assert pa.pa_decode_partition_size(cache, 256, 14, 2011, B) == B
+    # more sequences than the kernel keeps lengths of, a CUDA-core shape, fp32:
+    # the automatic rule
+    assert pa.pa_decode_partition_size(cache, 257, 14, 2011, B) == \
+        pa.pa_decode_partition_size(cache, 257, 14, 2011, -1)
+    mha = torch.zeros((2, 4, 16, 40, 128), dtype=torch.bfloat16, device="cuda")
+    assert pa.pa_decode_partition_size(mha, 32, 40, 2048, B) == 512
+    f32 = torch.zeros((2, 4, 16, 2, 64), dtype=torch.float32, device="cuda")
+    assert pa.pa_decode_partition_size(f32, 64, 14, 2011, B) == \
+        pa.pa_decode_partition_size(f32, 64, 14, 2011, -1)
+    # workspace: partials for min(ceil(len / 128), ceil(ranges / Hkv) + 1)
+    # per row, then one piece count per (sequence, KV head)
+    for (hkv, d, s, hq, max_len) in [(2, 64, 64, 14, 2011), (8, 128, 8, 32, 32768),
+                                     (1, 64, 3, 8, 100000)]:
+        c = torch.zeros((2, 4, 16, hkv, d), dtype=torch.bfloat16, device="cuda")
+        ranges = sms * (2 if d == 64 else 1)
+        mp = min(-(-max_len // 128), -(-ranges // hkv) + 1)
+        rows = s * hq * mp
+        up = lambda n: -(-n // 256) * 256
+        assert pa.pa_decode_workspace_size(c, s, hq, max_len, B) == \
+            256 + up(rows * d * 4) + up(rows * 4) + up(s * hkv * 4)
+
+
+# (Hq, Hkv, head_size, block_size, lengths): the balanced split's cuts
+BALANCED_SHAPES = [
+    # one long sequence among short ones: with fewer stages than ranges
+    # every stage is its own piece, and the long pair has 157 partials
+    (8, 1, 64, 16, [1] * 40 + [20000]),
+    # empty sequences among others, four KV heads (pieces span pairs)
+    (16, 4, 128, 16, [0, 129, 0, 3000, 1, 0, 7000]),
+    # everything fits in one stage per pair: one piece each, no partials
+    (14, 2, 64, 16, [5, 128, 1, 77]),
+    # many pairs per range: ranges cut pairs at arbitrary stages
+    (14, 2, 64, 16, [int(x) for x in np.random.default_rng(5).integers(1, 4000, size=200)]),
+    # the largest batch the split covers, with empty sequences
+    (14, 2, 64, 16, [int(x) * (i % 7 != 3) for i, x in
+                     enumerate(np.random.default_rng(6).integers(1, 600, size=256))]),
+    # groups of 16, block size 8 and 256
+    (32, 2, 64, 8, [3000, 5, 900, 129]),
+    (16, 16, 128, 256, [100, 256, 700, 5000]),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lens", BALANCED_SHAPES,
+                         ids=["hq%d_hkv%d_d%d_bs%d_n%d" % (s[0], s[1], s[2], s[3], len(s[4]))
+                              for s in BALANCED_SHAPES])
+def test_balanced_split(hq, hkv, d, bs, lens):
+    case = workloads.custom(len(lens), hq, hkv, d, bs, lens, "bf16",
+                            seed=hq * 31 + d + bs + len(lens), cache_fill="garbage")
+    ref, cache_ref = oracle_reference(case)
+    for fused in (False, True):
+        dc = DeviceCase(case)
+        out = (dc.step_fused if fused else dc.step)(pa.PA_PARTITION_BALANCED,
+                                                     kernel=pa.PA_KERNEL_TENSOR)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        assert np.array_equal(to_host_bits(dc.cache), cache_ref), "cache differs"
+        assert_close(to_f64(out), ref, "bf16", "balanced fused=%s" % fused)
+
+
+def test_balanced_split_is_deterministic():
+    case = workloads.custom(5, 14, 2, 64, 16, [100, 900, 2000, 1, 0], "bf16", seed=18)
+    dc = DeviceCase(case)
+    a = dc.step(pa.PA_PARTITION_BALANCED, kernel=pa.PA_KERNEL_TENSOR).clone()
+    b = dc.step(pa.PA_PARTITION_BALANCED, kernel=pa.PA_KERNEL_TENSOR).clone()
+    assert torch.equal(a, b)
 
 
 
@@ -239,7 +315,7 @@ def test_decode_with_fused_cache_write(hq, hkv, d, bs, lens, dtype, parts):
                             seed=hq * 100 + d + bs + 7, cache_fill="garbage")
     ref, cache_ref = oracle_reference(case)
     for kernel in kernels_for(case):
-        for p in parts:
+        for p in tuple(parts) + (pa.PA_PARTITION_BALANCED,):
             dc = DeviceCase(case)
             out = dc.step_fused(p, kernel=kernel)
             torch.cuda.synchronize()
