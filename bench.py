@@ -683,7 +683,10 @@ def main():
     ap.add_argument("--workload", default="qwen2_gqa")
     ap.add_argument("--partition", type=int, default=-1,
                     help="tokens per split-KV partition; 0 = no split, -1 = library's choice")
-    ap.add_argument("--graph", type=int, default=1, help="replay the step as CUDA graphs")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="replay the step as CUDA graphs (default: plain launches on the "
+                         "stream, chained by programmatic dependent launch; measured faster "
+                         "on GB300: 27.2 vs 28.0 us per Qwen2-shape step, e2e 41.8 vs 46.3)")
     ap.add_argument("--kernel", type=int, default=0,
                     help="decode kernel family: 0 = library's choice, 1 = CUDA cores, 2 = tensor cores")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
