@@ -1,80 +1,33 @@
 // Tensor-core (tcgen05) decode kernels: bf16, head sizes 64 and 128, query
-// groups up to 16; a persistent grid sized by occupancy.
-#include <algorithm>
-#include <atomic>
-
+// groups up to 16; a persistent grid sized by occupancy.  The kernels live
+// in one translation unit per (head size, timeline on or off).
 #include "decode_tc_kernel.cuh"
 #include "pa_launch.h"
 
 namespace pa {
 
-template <int D, int GP>
-static cudaError_t launch_tc(int num_sms, int smem_bytes, cudaStream_t stream,
-                             const CUtensorMap& kv_map, const CUtensorMap& q_map,
-                             const DecodeParams& params) {
-  static std::atomic<int> configured[64];
-  static std::atomic<int> per_sm[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (smem_bytes > configured[dev].load(std::memory_order_relaxed)) {
-    e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GP>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(paged_decode_tc_kernel<D, GP>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured[dev].store(smem_bytes, std::memory_order_relaxed);
-    // Resident CTAs per SM: bounded by shared memory (plus the 1 KB the
-    // driver reserves per CTA), registers and tensor-memory columns.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, paged_decode_tc_kernel<D, GP>);
-    if (e != cudaSuccess) return e;
-    int smem_per_sm = 0, regs_per_sm = 0;
-    e = cudaDeviceGetAttribute(&smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
-    if (e != cudaSuccess) return e;
-    const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;
-    int blocks = smem_per_sm / (smem_bytes + 1024);
-    blocks = std::min(blocks, regs_per_sm / (regs_per_warp * (kTcThreads / 32)));
-    blocks = std::min(blocks, 512 / kTcTmemCols);
-    per_sm[dev].store(blocks < 1 ? 1 : blocks, std::memory_order_relaxed);
-  }
-  // Persistent grid: as many CTAs as fit at once, at most one per work item.
-  long long grid = (long long)num_sms * per_sm[dev].load(std::memory_order_relaxed);
-  if (grid > params.total_items) grid = params.total_items;
-  if (grid < 1) return cudaSuccess;
-  DecodeParams prm = params;
-  if (prm.trace != nullptr &&
-      (size_t)grid * kTcTraceRoles * (size_t)prm.trace_per_role * 16 > (size_t)prm.trace_bytes)
-    prm.trace = nullptr;  // the buffer cannot hold this launch's timeline
-  void* args[] = {const_cast<CUtensorMap*>(&kv_map), const_cast<CUtensorMap*>(&q_map), &prm};
-  return launch_overlapped((const void*)paged_decode_tc_kernel<D, GP>, dim3((unsigned)grid),
-                           dim3(kTcThreads), (size_t)smem_bytes, stream, args);
-}
-
-template <int D>
-static cudaError_t launch_tc_group(int num_sms, int smem_bytes, cudaStream_t stream,
-                                   const CUtensorMap& kv_map, const CUtensorMap& q_map,
-                                   const DecodeParams& params) {
-  const int g = params.group;
-  if (g <= 1) return launch_tc<D, 1>(num_sms, smem_bytes, stream, kv_map, q_map, params);
-  if (g <= 2) return launch_tc<D, 2>(num_sms, smem_bytes, stream, kv_map, q_map, params);
-  if (g <= 4) return launch_tc<D, 4>(num_sms, smem_bytes, stream, kv_map, q_map, params);
-  if (g <= 8) return launch_tc<D, 8>(num_sms, smem_bytes, stream, kv_map, q_map, params);
-  return launch_tc<D, 16>(num_sms, smem_bytes, stream, kv_map, q_map, params);
-}
+#define PA_DECLARE_TC_UNIT(NAME)                                                       \
+  cudaError_t NAME(int, int, cudaStream_t, const CUtensorMap&, const CUtensorMap&, \
+                   const DecodeParams&);
+PA_DECLARE_TC_UNIT(launch_tc_d64)
+PA_DECLARE_TC_UNIT(launch_tc_d64_trace)
+PA_DECLARE_TC_UNIT(launch_tc_d128)
+PA_DECLARE_TC_UNIT(launch_tc_d128_trace)
+#undef PA_DECLARE_TC_UNIT
 
 cudaError_t launch_decode_tc(int head_size, int num_sms, int smem_bytes, cudaStream_t stream,
                              const CUtensorMap& kv_map, const CUtensorMap& q_map,
                              const DecodeParams& params, bool* supported) {
   *supported = true;
+  const DecodeParams& prm = params;
+  const bool trace = prm.trace != nullptr;  // the timeline kernels run only while one is set
   switch (head_size) {
-    case 64: return launch_tc_group<64>(num_sms, smem_bytes, stream, kv_map, q_map, params);
-    case 128: return launch_tc_group<128>(num_sms, smem_bytes, stream, kv_map, q_map, params);
+    case 64:
+      return trace ? launch_tc_d64_trace(num_sms, smem_bytes, stream, kv_map, q_map, prm)
+                   : launch_tc_d64(num_sms, smem_bytes, stream, kv_map, q_map, prm);
+    case 128:
+      return trace ? launch_tc_d128_trace(num_sms, smem_bytes, stream, kv_map, q_map, prm)
+                   : launch_tc_d128(num_sms, smem_bytes, stream, kv_map, q_map, prm);
     default: *supported = false; return cudaSuccess;
   }
 }

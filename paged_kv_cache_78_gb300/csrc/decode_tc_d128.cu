@@ -1,0 +1,2 @@
+#include "decode_tc_inst.cuh"
+PA_DEFINE_TC_UNIT(128, false, launch_tc_d128)

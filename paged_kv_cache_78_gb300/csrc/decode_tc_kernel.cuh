@@ -177,11 +177,13 @@ struct TcBars {
   }
 };
 
-// One event of the optional timeline (see pa_set_decode_trace).
+// One event of the optional timeline (see pa_set_decode_trace); compiled
+// only into the kernels launched while a timeline is requested.
+template <bool kTrace>
 __device__ __forceinline__ void tc_trace(const DecodeParams& p, int role, int& n, uint32_t tag,
                                          uint32_t arg) {
-  if (p.trace != nullptr) {
-    if (n < p.trace_per_role) {
+  if constexpr (kTrace) {
+    if (p.trace != nullptr && n < p.trace_per_role) {
       unsigned long long* e =
           p.trace + (((size_t)blockIdx.x * kTcTraceRoles + role) * (size_t)p.trace_per_role + n) * 2;
       e[0] = (unsigned long long)clock64();
@@ -219,7 +221,10 @@ __device__ __forceinline__ bool tc_epilogue(int gk, const TcBars& b, uint32_t t_
 
 // GP: the query group size G rounded up to a power of two (1..16); the
 // softmax warpgroup handles GP heads (the MMAs always compute 16 columns).
-template <int D, int GP>
+// kBal: the balanced split (else fixed partitions, or none); kTrace: record
+// the timeline.  Each is a separate kernel so that a launch carries only the
+// code it runs.
+template <int D, int GP, bool kBal, bool kTrace>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                            const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // counter); the producer loads its block-table window now, overlapping the
   // sequence-length loads below.
   int pf_win = -1, pf_s = -1, pf_cur = 0, pf_nxt = 0;
-  if (warp == 0 && !p.dense_items && !p.balanced && (int)blockIdx.x < p.total_items) {
+  if (!kBal && warp == 0 && !p.dense_items && (int)blockIdx.x < p.total_items) {
     const int sh = p.num_seqs * p.num_kv_heads;
     const int part = (int)blockIdx.x / sh;
     pf_s = ((int)blockIdx.x - part * sh) / p.num_kv_heads;
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int sh = p.num_seqs * p.num_kv_heads;
     const int P = p.partition_tokens;
     int gk = 0, qi = 0, ii = 0, ntr = 0;
-    if (lane == 0) tc_trace(p, 0, ntr, 9, p.trace ? (uint32_t)global_timer() : 0u);
+    if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 9, kTrace ? (uint32_t)global_timer() : 0u);
     // Dense numbering (many partitions per sequence, batches of up to
     // kTcLensCache): sequence s owns items pre[s] .. pre[s+1]-1, its
     // partitions in order with the KV heads fastest, so no index is spent on
@@ -356,7 +361,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // sequence s by CTA s mod grid.
     int* pre = reinterpret_cast<int*>(base + lay.pre_off);
     unsigned int total = (unsigned)p.total_items;
-    const bool bal = p.balanced && lens_s != nullptr;
+    // The balanced split needs the lengths in shared memory (the host
+    // launches it only for batches that fit); without them nothing is done.
+    constexpr bool bal = kBal;
+    if (kBal && lens_s == nullptr && blockIdx.x == 0 && lane == 0)
+      record_error(p.err, PA_DEVERR_SEQ_LEN);
     const bool dense = (p.dense_items || bal) && lens_s != nullptr;
     if (dense) {
       int carry = 0;
@@ -403,7 +412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       TcItem it{0, 0, 0, 0, 0, 0, 0, kItemEnd};
       bool skip = false;
       int wnew = 0;  // this item holds the sequence's newest token and writes it (fused write)
-      if (lane == 0 && bal) {
+      if (kBal && lane == 0 && lens_s != nullptr) {
         if (bg < bg_end) {
           // The sequence whose stages contain bg: the last s with pre[s] <= bg.
           int lo = 0, hi = p.num_seqs - 1;
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             zs += (int)gridDim.x;
           }
         }
-      } else if (lane == 0 && dense && idx < total) {
+      } else if (!kBal && lane == 0 && dense && idx < total) {
         // The sequence whose items contain idx: the last s with pre[s] <= idx.
         int lo = 0, hi = p.num_seqs - 1;
         while (lo < hi) {
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           it.final_out = nparts == 1;
           wnew = p.new_k != nullptr && it.tok1 == L;
         }
-      } else if (lane == 0 && !dense && idx < total) {
+      } else if (!kBal && lane == 0 && !dense && idx < total) {
         it.part = (int)(idx / (unsigned)sh);
         const int rem = (int)(idx % (unsigned)sh);
         it.s = rem / p.num_kv_heads;
@@ -508,11 +517,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wnew = p.new_k != nullptr && it.tok1 == L;
         }
       }
-      if (lane == 0) tc_trace(p, 0, ntr, 10, bal ? (uint32_t)bg : idx);
+      if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 10, bal ? (uint32_t)bg : idx);
       wnew = __shfl_sync(0xffffffffu, wnew, 0);
       skip = __shfl_sync(0xffffffffu, skip, 0);
       if (skip) {
-        if (lane == 0 && !bal) idx = gridDim.x + atomicAdd(p.sched, 1u);
+        if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
         continue;
       }
       it.s = __shfl_sync(0xffffffffu, it.s, 0);
@@ -539,7 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ring[j].final_out = it.final_out;
           ring[j].kind = it.kind;
           mbar_arrive(bars.it_full + 8u * j);
-          tc_trace(p, 0, ntr, 1, (uint32_t)ii);
+          tc_trace<kTrace>(p, 0, ntr, 1, (uint32_t)ii);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -549,10 +558,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       ++ii;
       if (it.kind == kItemEnd) {
-        if (lane == 0) tc_trace(p, 0, ntr, 8, (uint32_t)ii);
+        if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 8, (uint32_t)ii);
         break;
       }
-      if (lane == 0 && !bal) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
+      if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
       if (it.kind != kItemAttend) continue;
 
       // Query rows h*G .. h*G+15 of sequence s (rows past G are masked).
@@ -576,7 +585,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++qi;
       if (lane == 0) {
         flags[2] = qi;
-        tc_trace(p, 0, ntr, 11, (uint32_t)qi);
+        tc_trace<kTrace>(p, 0, ntr, 11, (uint32_t)qi);
       }
 
       // The item's K/V stages.  Every lane issues TMA boxes (a box = one
@@ -596,7 +605,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
       }
       pf_win = -1;
-      if (lane == 0) tc_trace(p, 0, ntr, 12, (uint32_t)(cur + nxt));
+      if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 12, (uint32_t)(cur + nxt));
       for (int k = 0; k < it.nstages; ++k, ++gk) {
         const int slot = gk % NS;
         if (gk >= NS) {
@@ -618,7 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)nbox * box_bytes);
-          tc_trace(p, 0, ntr, 20, (uint32_t)gk);
+          tc_trace<kTrace>(p, 0, ntr, 20, (uint32_t)gk);
         }
         __syncwarp();
         const uint32_t kdst = sbase + (uint32_t)slot * (uint32_t)lay.stage;
@@ -643,7 +652,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (lane == 0) {
           flags[1] = gk + 1;
-          tc_trace(p, 0, ntr, 2, (uint32_t)gk);
+          tc_trace<kTrace>(p, 0, ntr, 2, (uint32_t)gk);
         }
       }
       if (!ok) {
@@ -677,7 +686,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (leader) {
             mbar_arrive(bars.it_free + 8u * j);
-            tc_trace(p, 1, ntr, 13, (uint32_t)ii);
+            tc_trace<kTrace>(p, 1, ntr, 13, (uint32_t)ii);
           }
           ++ii;
           progress = true;
@@ -710,7 +719,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint64_t b0 = tc::smem_desc_sw128(p_s + (uint32_t)sb * 2u * kTcHeads * 128u, 16,
                                                   1024);
           if (leader) {
-            tc_trace(p, 1, ntr, 17, (uint32_t)gk);
+            tc_trace<kTrace>(p, 1, ntr, 17, (uint32_t)gk);
 #pragma unroll
             for (int kk = 0; kk < kPvSteps; ++kk) {
               const uint32_t aoff = (uint32_t)(kk * 2 * kChunkBytes);
@@ -719,7 +728,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc::mma_commit(bars.o_full + 8u * sb);
             tc::mma_commit(bars.empty0 + 8u * slot);
-            tc_trace(p, 1, ntr, 4, (uint32_t)gk);
+            tc_trace<kTrace>(p, 1, ntr, 4, (uint32_t)gk);
           }
           __syncwarp();
           ++next_pv;
@@ -748,7 +757,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc::mma_commit(bars.s_full + 8u * sb);
             if (last) tc::mma_commit(bars.q_free + 8u * qb);  // the item's Q tile is no longer read
-            tc_trace(p, 1, ntr, 3, (uint32_t)gk);
+            tc_trace<kTrace>(p, 1, ntr, 3, (uint32_t)gk);
           }
           __syncwarp();
           ++next_qk;
@@ -816,12 +825,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       it.nstages = ring[j].nstages;
       it.final_out = ring[j].final_out;
       it.kind = ring[j].kind;
-      if (lane == 0) tc_trace(p, warp, ntr, 21, (uint32_t)((warp << 16) | ii));
+      if (lane == 0) tc_trace<kTrace>(p, warp, ntr, 21, (uint32_t)((warp << 16) | ii));
       ok = softmax_group_all(w && ok && !flags[0]);  // every thread has read the entry
       if (!ok) break;
       if (tid == 64) {
         mbar_arrive(bars.it_free + 8u * j);
-        tc_trace(p, 2, ntr, 14, (uint32_t)ii);
+        tc_trace<kTrace>(p, 2, ntr, 14, (uint32_t)ii);
       }
       if (it.kind == kItemEnd) break;
       const size_t row0 = (size_t)it.s * p.num_heads + (size_t)it.h * G;
@@ -846,7 +855,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int sb = g_k & 1;
         const int slot = g_k % NS;
         const bool ws = mbar_wait_bounded(bars.s_full + 8u * sb, (g_k >> 1) & 1, p.err);
-        if (tid == 64) tc_trace(p, 2, ntr, 15, (uint32_t)g_k);
+        if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 15, (uint32_t)g_k);
         __syncwarp();
         tc::fence_after_sync();
         float sc[GP];
@@ -854,7 +863,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::tmem_wait_ld();
         tc::fence_before_sync();
         mbar_arrive(bars.s_free + 8u * sb);
-        if (tid == 64) tc_trace(p, 2, ntr, 5, (uint32_t)g_k);
+        if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 5, (uint32_t)g_k);
 
         const int nvalid = min(kTcTokens, it.tok1 - (it.tok0 + k * kTcTokens));
         const bool valid = row < nvalid;
@@ -926,11 +935,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_proxy_async_smem();
         mbar_arrive(bars.p_full + 8u * sb);
-        if (tid == 64) tc_trace(p, 2, ntr, 6, (uint32_t)g_k);
-        else if (lane == 0) tc_trace(p, warp, ntr, 19, (uint32_t)((warp << 16) | g_k));
+        if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 6, (uint32_t)g_k);
+        else if (lane == 0) tc_trace<kTrace>(p, warp, ntr, 19, (uint32_t)((warp << 16) | g_k));
         if (k >= 1) {
           ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, o_acc, alpha_prev) && ok;
-          if (tid == 64) tc_trace(p, 2, ntr, 16, (uint32_t)(g_k - 1));
+          if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(g_k - 1));
         }
 #pragma unroll
         for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
@@ -940,7 +949,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // warp executes the tensor-memory load convergently or not at all.
       if (!(ok = softmax_group_all(ok && !flags[0]))) break;
       ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, o_acc, alpha_prev);
-      if (tid == 64) tc_trace(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
+      if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
       gk += n;
 
       // l over the warpgroup's 128 token rows, then the item's output.
@@ -982,8 +991,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!it.final_out && q4 == 0 && lane < G)
           p.part_lse[(row0 + lane) * (size_t)p.max_parts + it.part] = m_l + log2f(lsum_l);
       }
-      if (tid == 64) tc_trace(p, 2, ntr, 7, (uint32_t)ii);
-      else if (lane == 0) tc_trace(p, warp, ntr, 22, (uint32_t)((warp << 16) | ii));
+      if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 7, (uint32_t)ii);
+      else if (lane == 0) tc_trace<kTrace>(p, warp, ntr, 22, (uint32_t)((warp << 16) | ii));
     }
     if (!ok) flags[0] = 1;
   }
