@@ -193,6 +193,16 @@ __device__ __forceinline__ void tc_trace(const DecodeParams& p, int role, int& n
   }
 }
 
+// floor(a / b) for 0 <= a < 2^24 and b >= 1, from a float reciprocal of b:
+// the product is within one of the quotient, and one step corrects it.
+__device__ __forceinline__ int div_by_recip(int a, int b, float inv_b) {
+  int q = __float2int_rz(__int2float_rn(a) * inv_b);
+  const int r = a - q * b;
+  if (r >= b) ++q;
+  else if (r < 0) --q;
+  return q;
+}
+
 __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -397,10 +407,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       total = (unsigned)carry;
     }
     unsigned int idx = blockIdx.x;
-    // Balanced split cursor (lane 0): stages [bg, bg_end) of range brange,
-    // then sequence zs (KV head zh) of the zero-stage pass.
+    // Balanced split cursor (every lane holds the same): stages [bg, bg_end)
+    // of range brange, then sequence zs (KV head zh) of the zero-stage pass.
+    // Stage counts stay below 2^24 there (the reciprocal divisions need it;
+    // beyond, no work is done and the length error is recorded).
     const int ranges = p.total_items;
     const int bq = bal ? max(1, (int)((total + (unsigned)ranges - 1) / (unsigned)ranges)) : 1;
+    const float inv_bq = 1.f / (float)bq;
+    if (kBal && total >= (1u << 24)) {
+      if (blockIdx.x == 0 && lane == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
+      total = 0;
+    }
     int brange = (int)blockIdx.x, bg = 0, bg_end = 0, zs = (int)blockIdx.x, zh = 0;
     if (bal && brange < ranges) {
       bg = brange * bq;
@@ -412,32 +429,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       TcItem it{0, 0, 0, 0, 0, 0, 0, kItemEnd};
       bool skip = false;
       int wnew = 0;  // this item holds the sequence's newest token and writes it (fused write)
-      if (kBal && lane == 0 && lens_s != nullptr) {
+      if (kBal && lens_s != nullptr) {
+        // Warp-uniform: every lane computes the same item, lane 0 writes.
         if (bg < bg_end) {
-          // The sequence whose stages contain bg: the last s with pre[s] <= bg.
-          int lo = 0, hi = p.num_seqs - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (pre[mid] <= bg) lo = mid; else hi = mid - 1;
-          }
+          // The sequence whose stages contain bg: the last s with
+          // pre[s] <= bg (pre is non-decreasing, so count the s that qualify).
+          int lo = -1;
+          for (int c0 = 0; c0 < p.num_seqs; c0 += 32)
+            lo += __popc(__ballot_sync(0xffffffffu, c0 + lane < p.num_seqs && pre[c0 + lane] <= bg));
           const int L = lens_s[lo];
           const int n = (L + kTcTokens - 1) / kTcTokens;  // stages of each of its pairs
           const int off = bg - pre[lo];
-          const int h = off / n;
+          const int h = div_by_recip(off, n, 1.f / (float)n);
           const int k0 = off - h * n;
           const int len = min(n - k0, bg_end - bg);
           const int pair0 = pre[lo] + h * n;  // the pair's first stage
-          const int first = pair0 / bq;
-          const int npieces = (pair0 + n - 1) / bq - first + 1;
+          const int first = div_by_recip(pair0, bq, inv_bq);
+          const int npieces = div_by_recip(pair0 + n - 1, bq, inv_bq) - first + 1;
           it.s = lo;
           it.h = h;
-          it.part = bg / bq - first;
+          it.part = div_by_recip(bg, bq, inv_bq) - first;
           it.tok0 = k0 * kTcTokens;
           it.tok1 = min(L, (k0 + len) * kTcTokens);
           it.nstages = len;
           it.final_out = npieces == 1;
           it.kind = kItemAttend;
-          if (it.part == 0) {
+          if (it.part == 0 && lane == 0) {
             p.part_counts[lo * p.num_kv_heads + h] = npieces <= p.max_parts ? npieces : 0;
             if (npieces > p.max_parts) record_error(p.err, PA_DEVERR_SEQ_LEN);
           }
@@ -455,7 +472,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (pre[zs + 1] == pre[zs]) {
             // No stages: zero rows for length 0 (a length error leaves its
             // rows undefined); no partials either way.
-            p.part_counts[zs * p.num_kv_heads + zh] = 0;
+            if (lane == 0) p.part_counts[zs * p.num_kv_heads + zh] = 0;
             it.s = zs;
             it.h = zh;
             it.kind = kItemZero;
@@ -518,20 +535,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 10, bal ? (uint32_t)bg : idx);
-      wnew = __shfl_sync(0xffffffffu, wnew, 0);
-      skip = __shfl_sync(0xffffffffu, skip, 0);
+      if constexpr (!kBal) {
+        wnew = __shfl_sync(0xffffffffu, wnew, 0);
+        skip = __shfl_sync(0xffffffffu, skip, 0);
+      }
       if (skip) {
         if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
         continue;
       }
-      it.s = __shfl_sync(0xffffffffu, it.s, 0);
-      it.h = __shfl_sync(0xffffffffu, it.h, 0);
-      it.part = __shfl_sync(0xffffffffu, it.part, 0);
-      it.tok0 = __shfl_sync(0xffffffffu, it.tok0, 0);
-      it.tok1 = __shfl_sync(0xffffffffu, it.tok1, 0);
-      it.nstages = __shfl_sync(0xffffffffu, it.nstages, 0);
-      it.final_out = __shfl_sync(0xffffffffu, it.final_out, 0);
-      it.kind = __shfl_sync(0xffffffffu, it.kind, 0);
+      if constexpr (!kBal) {
+        it.s = __shfl_sync(0xffffffffu, it.s, 0);
+        it.h = __shfl_sync(0xffffffffu, it.h, 0);
+        it.part = __shfl_sync(0xffffffffu, it.part, 0);
+        it.tok0 = __shfl_sync(0xffffffffu, it.tok0, 0);
+        it.tok1 = __shfl_sync(0xffffffffu, it.tok1, 0);
+        it.nstages = __shfl_sync(0xffffffffu, it.nstages, 0);
+        it.final_out = __shfl_sync(0xffffffffu, it.final_out, 0);
+        it.kind = __shfl_sync(0xffffffffu, it.kind, 0);
+      }
+      // The item's block-table window, loaded now so that its latency
+      // overlaps the item's publication and query load: [win, win+32) in
+      // `cur`, [win+32, win+64) in `nxt` (a stage spans at most 16 blocks).
+      const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+      const int lb_end = (it.tok1 + BS - 1) >> l2bs;
+      int win = it.tok0 >> l2bs;
+      int cur, nxt;
+      if (win == pf_win && it.s == pf_s) {  // the first item's window, loaded early
+        cur = pf_cur;
+        nxt = pf_nxt;
+      } else {
+        cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
+        nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+      }
+      pf_win = -1;
       // Publish it in the ring.
       const int j = ii % kTcItemRing;
       bool ok = true;
@@ -590,21 +626,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       // The item's K/V stages.  Every lane issues TMA boxes (a box = one
       // block's rows of one 128-byte column group of K or of V): one thread
-      // issuing them in sequence cannot keep HBM busy.  The block table is
-      // cached in two 32-entry register windows, [win, win+32) in `cur` and
-      // [win+32, win+64) in `nxt`; a stage spans at most 16 blocks.
-      const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
-      const int lb_end = (it.tok1 + BS - 1) >> l2bs;
-      int win = it.tok0 >> l2bs;
-      int cur, nxt;
-      if (win == pf_win && it.s == pf_s) {  // the first item's window, loaded early
-        cur = pf_cur;
-        nxt = pf_nxt;
-      } else {
-        cur = (win + lane < lb_end) ? __ldg(table + win + lane) : 0;
-        nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
-      }
-      pf_win = -1;
+      // issuing them in sequence cannot keep HBM busy.
       if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 12, (uint32_t)(cur + nxt));
       for (int k = 0; k < it.nstages; ++k, ++gk) {
         const int slot = gk % NS;
