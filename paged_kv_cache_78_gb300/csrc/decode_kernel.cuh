@@ -484,6 +484,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 // CTA; each lane owns D/32 output columns and walks the row's partitions
 // with four loads in flight.  Same arithmetic as lse_reduce_kernel.
 constexpr int kReduceRowParts = 16;
+constexpr int kReduceRowSpec = 4;  // partials loaded before the row's count is known
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
@@ -499,6 +500,23 @@ __global__ void __launch_bounds__(256)
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   grid_dependency_wait();
   if (row >= (long long)num_seqs * num_heads) return;
+  // Every load of a row of up to kReduceRowSpec partials is issued at once,
+  // before the row's partial count arrives (one round trip instead of
+  // three): the count, lane q's log-sum-exp and the first partials'
+  // columns.  Slots past the count hold stale values and are masked.
+  const float* lse = part_lse + (size_t)row * max_parts;
+  const float* po = part_o + (size_t)row * max_parts * D + lane * kPer;
+  const float lse_l = lane < max_parts ? lse[lane] : -INFINITY;
+  float v0[kReduceRowSpec][kPer];
+#pragma unroll
+  for (int q = 0; q < kReduceRowSpec; ++q)
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+      float2 t = make_float2(0.f, 0.f);
+      if (q < max_parts) t = *reinterpret_cast<const float2*>(po + (size_t)q * D + e);
+      v0[q][e] = t.x;
+      v0[q][e + 1] = t.y;
+    }
   int nparts;
   if (counts != nullptr) {
     nparts = counts[row / group];  // pieces of the row's (sequence, KV head) pair
@@ -507,16 +525,20 @@ __global__ void __launch_bounds__(256)
     nparts = L <= 0 ? 0 : (L + partition_tokens - 1) / partition_tokens;
   }
   if (nparts <= 1 || nparts > max_parts) return;  // written by the decode kernel (or an error)
-  const float* lse = part_lse + (size_t)row * max_parts;
-  const float* po = part_o + (size_t)row * max_parts * D + lane * kPer;
-  float M = lane < nparts ? lse[lane] : -INFINITY;
-  M = warp_max(M);
-  float w_own = lane < nparts ? fast_exp2(lse[lane] - M) : 0.f;
+  const float M = warp_max(lane < nparts ? lse_l : -INFINITY);
+  float w_own = lane < nparts ? fast_exp2(lse_l - M) : 0.f;
   const float wsum = warp_sum(w_own);
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  for (int q = 0; q < nparts; ++q) {
+#pragma unroll
+  for (int q = 0; q < kReduceRowSpec; ++q) {
+    const float w = __shfl_sync(0xffffffffu, w_own, q);
+    if (q < nparts)  // a stale slot may hold anything, even NaN
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, v0[q][e], acc[e]);
+  }
+  for (int q = kReduceRowSpec; q < nparts; ++q) {
     const float w = __shfl_sync(0xffffffffu, w_own, q);
     float v[kPer];
 #pragma unroll
