@@ -285,6 +285,41 @@ def test_balanced_split(hq, hkv, d, bs, lens):
         assert_close(to_f64(out), ref, "bf16", "balanced fused=%s" % fused)
 
 
+@pytest.mark.parametrize("hkv,d,lens", [
+    (2, 64, None),                                   # the Qwen2-shaped batch
+    (8, 128, [3000] * 8),                            # long sequences, equal lengths
+    (4, 128, [0, 1, 700, 3000, 129, 0, 5000, 64]),   # empty sequences between others
+])
+def test_balanced_split_piece_counts_follow_the_rule(hkv, d, lens):
+    # The kernel records each (sequence, KV head) pair's piece count in the
+    # workspace (after the partials); it must be the number of stage ranges
+    # the pair meets: stages laid end to end, cut every ceil(total / ranges).
+    if lens is None:
+        case = workloads.qwen2_gqa()
+    else:
+        case = workloads.custom(len(lens), 4 * hkv, hkv, d, 16, lens, "bf16", seed=51)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ranges = sms * (2 if d == 64 else 1)
+    dc = DeviceCase(case)
+    nbytes = pa.pa_decode_workspace_size(dc.cache, case.num_seqs, case.num_heads,
+                                         case.max_seq_len, pa.PA_PARTITION_BALANCED)
+    ws = pa.alloc_workspace(nbytes, "cuda")
+    dc.step(pa.PA_PARTITION_BALANCED, workspace=ws, kernel=pa.PA_KERNEL_TENSOR)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    pairs = case.num_seqs * case.num_kv_heads
+    region = -(-pairs * 4 // 256) * 256
+    counts = ws[nbytes - region:nbytes - region + pairs * 4].view(torch.int32).cpu().numpy()
+    n = (case.seq_lens.astype(np.int64) + 127) // 128
+    per_pair = np.repeat(n, case.num_kv_heads)
+    q = max(1, -(-int(per_pair.sum()) // ranges))
+    start = np.concatenate([[0], np.cumsum(per_pair)[:-1]])
+    want = np.where(per_pair > 0, (start + per_pair - 1) // q - start // q + 1, 0)
+    assert np.array_equal(counts, want)
+    # every CTA's range holds at most q stages: the split is balanced
+    assert q == max(1, -(-int(per_pair.sum()) // ranges))
+
+
 def test_balanced_split_is_deterministic():
     case = workloads.custom(5, 14, 2, 64, 16, [100, 900, 2000, 1, 0], "bf16", seed=18)
     dc = DeviceCase(case)
