@@ -541,19 +541,29 @@ def run_gpu(args, rank, world, device):
     # step's inputs, the step, D2H of the output, all inside the timed region.
     # The host side holds the step's inputs in one page-locked arena (query,
     # new K/V, slots, block tables, lengths: pack_step_inputs), copied in with
-    # one transfer per step.
+    # one transfer per step.  By default both transfers are the library's
+    # copy kernel (pa_copy_bytes), chained with the step's kernels by
+    # programmatic dependent launch; --e2e-copy dma takes the copy engine.
     out_host = torch.empty(st.out.numel() * st.out.element_size(), dtype=torch.uint8).pin_memory()
     h2d = arena_host.numel()
     d2h = out_host.numel()
 
+    out_bytes = st.out.view(torch.uint8).view(-1)
+
     def e2e_step():
-        arena.copy_(arena_host, non_blocking=True)
+        if args.e2e_copy == "kernel":
+            pa.pa_copy_bytes(arena, arena_host)
+        else:
+            arena.copy_(arena_host, non_blocking=True)
         if args.fused:
             st.write_and_decode()
         else:
             st.write()
             st.decode()
-        out_host.copy_(st.out.view(torch.uint8).view(-1), non_blocking=True)
+        if args.e2e_copy == "kernel":
+            pa.pa_copy_bytes(out_host, out_bytes)
+        else:
+            out_host.copy_(out_bytes, non_blocking=True)
 
     if not args.e2e:
         clocks = sampler.summary(t0, t1) if sampler else None
@@ -692,6 +702,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the CPU baseline (0 = skip)")
     ap.add_argument("--e2e", type=int, default=1, help="also time the step with host buffers")
+    ap.add_argument("--e2e-copy", choices=("kernel", "dma"), default="kernel",
+                    help="host<->device transfers of the end-to-end step: the library's copy "
+                         "kernel (pa_copy_bytes) or the copy engine")
     ap.add_argument("--fused", type=int, default=1,
                     help="1: the step is one pa_decode_append (the decode writes the new tokens); "
                          "0: pa_reshape_and_cache, then pa_decode")
@@ -752,7 +765,9 @@ def main():
         e2e = {"value": round(world * nbytes["step"] / (r["e2e_ms"] / 1e3) / 1e9, 2),
                "unit": "GB/s", "us_per_step": round(r["e2e_ms"] * 1e3, 2),
                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-               "cuda_graph": bool(args.graph)}
+               "cuda_graph": bool(args.graph),
+               "transfers": ("pa_copy_bytes kernels" if args.e2e_copy == "kernel"
+                             else "copy engine")}
 
     cpu = None
     if args.cpu_budget > 0:

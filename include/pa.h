@@ -130,6 +130,22 @@ pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const v
                          void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Copy `bytes` bytes from src to dst with a kernel on `stream`.  Each of dst
+ * and src is device memory or page-locked host memory (read or written
+ * through its device mapping, over NVLink-C2C on GB300); pageable host
+ * memory returns PA_ERR_INVALID_ARG and launches nothing, and so do
+ * overlapping ranges.  This is how a serving step's host-side inputs (the
+ * new tokens' query, K and V, slot mapping, block tables and lengths) come
+ * in and its attention output goes out: as a kernel, the copy chains with
+ * pa_reshape_and_cache and pa_decode by programmatic dependent launch, where
+ * a copy-engine transfer would stop the chain on both sides.  Any size and
+ * alignment; 16-byte aligned pointers on both sides move 16 bytes per load.
+ * bytes == 0 is a no-op.  Asynchronous on `stream`: the host side may be
+ * reused (src) or read (dst) only after the stream has passed the copy.
+ * ------------------------------------------------------------------------- */
+pa_status pa_copy_bytes(void* dst, const void* src, size_t bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Paged decode attention: one query token per sequence against the
  * sequence's cached tokens, block by block through its block table
  * (studying-code.tistory.com/16, section "PagedAttention: 운영체제의 페이징

@@ -49,7 +49,7 @@ EXPORTS = (
     "pa_version", "pa_set_decode_trace", "pa_pool_add_seq_tokens", "pa_pool_append_token_id",
     "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache", "pa_pool_usage",
     "pa_swap_blocks", "pa_pool_set_cpu_blocks", "pa_pool_swap_out", "pa_pool_swap_in",
-    "pa_pool_is_swapped", "pa_pool_num_free_cpu", "pa_decode_append",
+    "pa_pool_is_swapped", "pa_pool_num_free_cpu", "pa_decode_append", "pa_copy_bytes",
 )
 
 
@@ -109,6 +109,7 @@ def _load() -> ctypes.CDLL:
         "pa_pool_reset_prefix_cache": [vp],
         "pa_pool_usage": [vp, p_i64, p_i64],
         "pa_swap_blocks": [vp, desc, vp, desc, vp, i32, vp],
+        "pa_copy_bytes": [vp, vp, sz, vp],
         "pa_pool_set_cpu_blocks": [vp, i32],
         "pa_pool_swap_out": [vp, vp, i32, vp, p_i32],
         "pa_pool_swap_in": [vp, vp, i32, vp, p_i32],
@@ -229,6 +230,18 @@ def _dev_or_pinned_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
     if dtype is not None and t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     return t.data_ptr()
+
+
+def pa_copy_bytes(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Copy src's bytes into dst with a library kernel; either side may be
+    page-locked host memory.  Both contiguous, with the same byte size."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src differ in byte size")
+    if nbytes == 0:
+        return
+    _check(lib.pa_copy_bytes(_dev_or_pinned_ptr(dst, "dst"), _dev_or_pinned_ptr(src, "src"),
+                             nbytes, _stream(stream)), "pa_copy_bytes")
 
 
 def pa_swap_blocks(dst_cache: torch.Tensor, src_cache: torch.Tensor, pairs: torch.Tensor,

@@ -365,6 +365,22 @@ pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const v
                                             block_bytes, err, static_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_copy_bytes(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return PA_OK;
+  if (!dst || !src || bytes > ((size_t)1 << 40)) return PA_ERR_INVALID_ARG;
+  const void* d = nullptr;
+  const void* s = nullptr;
+  pa_status st = kernel_address(dst, &d);
+  if (st != PA_OK) return st;
+  if ((st = kernel_address(src, &s)) != PA_OK) return st;
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(d), s0 = reinterpret_cast<uintptr_t>(s);
+  if (d0 < s0 + bytes && s0 < d0 + bytes) return PA_ERR_INVALID_ARG;  // overlapping ranges
+  int sms = 0;
+  if ((st = device_state(nullptr, &sms)) != PA_OK) return st;
+  return cuda_status(pa::launch_copy_bytes(const_cast<void*>(d), s, (int64_t)bytes, sms,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs,
                                    int32_t num_heads, int32_t max_seq_len,
                                    int32_t partition_size, int32_t* resolved) {

@@ -82,6 +82,40 @@ __global__ void copy_blocks_kernel(uint8_t* __restrict__ dst_cache,
   for (; i < n16; i += step) stg_v4(d + i * 16, ldg_nc_v4(s + i * 16));
 }
 
+// Plain byte copy between any two addresses the GPU reaches (device memory,
+// page-locked host memory through its mapping).  A kernel rather than a copy
+// engine so that it chains with the neighbouring launches by programmatic
+// dependent launch: the step's host-side inputs come in and its output goes
+// out without the copy engine's own start-up on the stream.  Both sides
+// 16-byte aligned: 16-byte vectors, four in flight per thread, then the
+// ragged tail byte by byte; otherwise byte by byte throughout.
+__global__ void copy_bytes_kernel(uint8_t* __restrict__ dst, const uint8_t* src,
+                                  int64_t bytes, int vec) {
+  grid_dependents_launch();
+  grid_dependency_wait();
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t done = 0;
+  if (vec) {
+    const int64_t n16 = bytes / 16;
+    int64_t i = t;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (; i + 3 * step < n16; i += 4 * step) {
+      const uint4 a = __ldcg(s4 + i);
+      const uint4 b = __ldcg(s4 + i + step);
+      const uint4 c = __ldcg(s4 + i + 2 * step);
+      const uint4 e = __ldcg(s4 + i + 3 * step);
+      stg_v4(dst + i * 16, a);
+      stg_v4(dst + (i + step) * 16, b);
+      stg_v4(dst + (i + 2 * step) * 16, c);
+      stg_v4(dst + (i + 3 * step) * 16, e);
+    }
+    for (; i < n16; i += step) stg_v4(dst + i * 16, __ldcg(s4 + i));
+    done = n16 * 16;
+  }
+  for (int64_t i = done + t; i < bytes; i += step) dst[i] = __ldcg(src + i);
+}
+
 cudaError_t launch_reshape_and_cache(void* cache, const void* key, const void* value,
                                      const int64_t* slot_mapping, int64_t num_tokens,
                                      int64_t num_slots, int row_bytes, int64_t plane_bytes,
@@ -114,6 +148,21 @@ cudaError_t launch_copy_blocks(void* dst_cache, const void* src_cache, const int
   void* args[] = {&d, &s, &pairs, &dst_blocks, &src_blocks, &block_bytes, &dst_plane, &src_plane,
                   &err};
   return launch_overlapped((const void*)copy_blocks_kernel, grid, dim3(block), 0, stream, args);
+}
+
+cudaError_t launch_copy_bytes(void* dst, const void* src, int64_t bytes, int num_sms,
+                              cudaStream_t stream) {
+  const int block = 256;
+  const int vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15) == 0;
+  const int64_t units = vec ? bytes / 16 : bytes;
+  int64_t grid = (units + block - 1) / block;
+  if (grid > 2 * (int64_t)num_sms) grid = 2 * (int64_t)num_sms;
+  if (grid < 1) grid = 1;
+  uint8_t* d = static_cast<uint8_t*>(dst);
+  const uint8_t* s = static_cast<const uint8_t*>(src);
+  void* args[] = {&d, &s, &bytes, const_cast<int*>(&vec)};
+  return launch_overlapped((const void*)copy_bytes_kernel, dim3((unsigned)grid), dim3(block), 0,
+                           stream, args);
 }
 
 }  // namespace pa

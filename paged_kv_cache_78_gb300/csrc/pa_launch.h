@@ -38,6 +38,10 @@ cudaError_t launch_copy_blocks(void* dst_cache, const void* src_cache, const int
                                int num_pairs, int64_t dst_blocks, int64_t src_blocks,
                                int64_t block_bytes, unsigned int* err, cudaStream_t stream);
 
+// Byte copy by a kernel (device or page-locked host memory on either side).
+cudaError_t launch_copy_bytes(void* dst, const void* src, int64_t bytes, int num_sms,
+                              cudaStream_t stream);
+
 // Decode launchers, one per element type.  `supported` is set to false (and
 // nothing launched) when no kernel exists for (head_size, group).
 cudaError_t launch_decode_bf16(int head_size, int group, dim3 grid, int smem_bytes,

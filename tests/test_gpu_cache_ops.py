@@ -156,3 +156,43 @@ def test_swap_refuses_pageable_host_memory():
     assert st == pa.PA_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("nbytes,dst_off,src_off", [
+    (1, 0, 0), (15, 0, 0), (16, 0, 0), (17, 0, 0), (4096 + 3, 0, 0),
+    ((1 << 20) + 5, 0, 0), ((1 << 22) + 48, 16, 32),      # vectors, 4 in flight, ragged tail
+    (1000, 1, 0), (70001, 3, 5),                          # misaligned: byte by byte
+])
+@pytest.mark.parametrize("route", ["h2d", "d2h", "d2d", "h2h"])
+def test_copy_bytes_bit_exact(nbytes, dst_off, src_off, route):
+    # Every byte of the range arrives; the bytes around it keep their canary.
+    rng = np.random.default_rng(nbytes + dst_off + src_off)
+    src_np = rng.integers(0, 256, size=nbytes + src_off + 64, dtype=np.uint8)
+    dst_np = rng.integers(0, 256, size=nbytes + dst_off + 64, dtype=np.uint8)
+
+    def place(a, where):
+        t = torch.from_numpy(a)
+        return t.pin_memory() if where == "h" else t.cuda()
+
+    src = place(src_np, route[0])
+    dst = place(dst_np.copy(), route[-1])
+    pa.pa_copy_bytes(dst[dst_off:dst_off + nbytes], src[src_off:src_off + nbytes])
+    torch.cuda.synchronize()
+    expect = dst_np.copy()
+    expect[dst_off:dst_off + nbytes] = src_np[src_off:src_off + nbytes]
+    assert np.array_equal(dst.cpu().numpy(), expect)
+
+
+def test_copy_bytes_refuses_pageable_and_overlapping_ranges():
+    dev = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    pageable = torch.zeros(4096, dtype=torch.uint8)
+    assert pa.lib.pa_copy_bytes(dev.data_ptr(), pageable.data_ptr(), 4096, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_copy_bytes(pageable.data_ptr(), dev.data_ptr(), 4096, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_copy_bytes(dev.data_ptr() + 16, dev.data_ptr(), 64, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_copy_bytes(dev.data_ptr(), dev.data_ptr() + 64, 64, None) == pa.PA_OK
+    assert pa.lib.pa_copy_bytes(dev.data_ptr(), None, 0, None) == pa.PA_OK
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0

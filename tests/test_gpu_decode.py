@@ -357,3 +357,50 @@ def test_decode_with_fused_cache_write(hq, hkv, d, bs, lens, dtype, parts):
             assert pa.pa_get_device_error() == 0
             assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
             assert_close(to_f64(out), ref, case.dtype, "fused kernel=%d partition=%s" % (kernel, p))
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_steps_through_host_buffers(fused):
+    # A serving loop's form: each step's inputs come from page-locked host
+    # memory through pa_copy_bytes, the step runs, and its output goes back to
+    # page-locked host memory the same way, all chained on one stream with
+    # no synchronisation between steps.  Step i's query is the base query
+    # times a power of two, so each step's output is checked bit for bit
+    # against the same step on device-resident inputs, and step 0 against
+    # the oracle: an input copy that overtook the previous step's decode, or
+    # an output copy that overtook its own, would show.
+    lens = [1, 15, 16, 17, 33, 255, 700, 2048, 129, 1000]
+    case = workloads.custom(len(lens), 14, 2, 64, 16, lens, "bf16", seed=808,
+                            cache_fill="garbage")
+    ref, _ = oracle_reference(case)
+    dc = DeviceCase(case)
+    factors = (1.0, 2.0, 0.5, 4.0)
+    base_q = dc.query.clone()
+    want = []
+    for f in factors:
+        dc.query.copy_(base_q * f)
+        want.append((dc.step_fused() if fused else dc.step()).clone())
+    torch.cuda.synchronize()
+    assert_close(to_f64(want[0]), ref, case.dtype, "device-resident step")
+    # Host-side inputs of every step, and the device buffers they land in.
+    names = ("query", "block_tables", "seq_lens") + (
+        ("new_keys", "new_values") if fused else ("step_keys", "step_values", "step_slots"))
+    host = [{n: (base_q * f if n == "query" else getattr(dc, n)).cpu().pin_memory()
+             for n in names} for f in factors]
+    for n in names:
+        getattr(dc, n).view(torch.uint8).fill_(0x7f)
+    outs = [torch.full(tuple(base_q.shape), 7.0, dtype=base_q.dtype).pin_memory()
+            for _ in factors]
+    nbytes = pa.pa_decode_workspace_size(dc.cache, case.num_seqs, case.num_heads,
+                                         case.max_seq_len, -1)
+    ws = pa.alloc_workspace(nbytes, "cuda")
+    for i in range(len(factors)):
+        for n in names:
+            pa.pa_copy_bytes(getattr(dc, n), host[i][n])
+        out = dc.step_fused(workspace=ws) if fused else dc.step(workspace=ws)
+        pa.pa_copy_bytes(outs[i], out)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    for i in range(len(factors)):
+        assert torch.equal(outs[i].view(torch.int16), want[i].cpu().view(torch.int16)), \
+            "step %d through host buffers differs" % i
