@@ -172,6 +172,12 @@ pa_status resolve_partition(const pa_cache_desc* d, int num_seqs, int num_heads,
       p = 512;
       while (p > 64 && p > d->block_size && heads * ((max_seq_len + p - 1) / p) < 6LL * num_sms)
         p >>= 1;
+      // Batches the kernel takes longest first, with (sequence, KV head)
+      // pairs for four CTAs per SM and no sequence past 2048 tokens: no
+      // split.  The long sequences start first and the short ones fill the
+      // tail, with no partials and no reduce.
+      if (num_seqs <= pa::kLongestFirstMaxSeqs && heads >= 4LL * num_sms && max_seq_len <= 2048)
+        p = 0;
     }
     if (p > 0 && p < d->block_size) p = d->block_size;
   } else if (p < PA_PARTITION_BALANCED) {
@@ -576,6 +582,11 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     }
     prm.stage_bytes = stage_bytes;
     prm.stage_area = area_for(ns);
+    // Unsplit batches are taken longest first (with a split the partitions
+    // are of equal length but for the last, and the CTAs past a sequence's
+    // end would pay for the ranking).  The lengths to rank fit in one stage
+    // (at least 2 KB).
+    prm.longest_first = num_seqs <= pa::kLongestFirstMaxSeqs && part == 0;
     smem = pa::decode_smem_bytes(prm.stage_area, group, D);
   }
   if (smem > kMaxSmemPerCta) return PA_ERR_UNSUPPORTED;

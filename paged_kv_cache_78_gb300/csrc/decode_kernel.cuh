@@ -43,6 +43,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
 constexpr int kStageTokens = 32;
 constexpr int kPStride = 8;  // floats per token in the per-warp softmax-weight buffer
+constexpr int kLongestFirstMaxSeqs = 128;  // batches the CUDA-core kernel ranks by length
 
 struct DecodeParams {
   void* out;                    // [S][Hq][D] of T (final rows)
@@ -56,6 +57,7 @@ struct DecodeParams {
   int total_items;              // tensor-core kernel: num_seqs * num_kv_heads * max_parts
                                 // (balanced split: the number of stage ranges)
   int dense_items;              // tensor-core kernel: number only the real work items
+  int longest_first;            // CUDA-core kernel: grid z is a rank in decreasing length order
   int balanced;                 // tensor-core kernel: stage-balanced split (ranges of stages)
   int32_t* part_counts;         // balanced split: [S][Hkv] pieces of each pair (1 = final rows)
   int num_seqs;
@@ -130,13 +132,43 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
   const int part = blockIdx.x;
   const int h = blockIdx.y;
-  const int s = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   grid_dependency_wait();
-  const int L = p.seq_lens[s];
+  int s = blockIdx.z;
+  int L;
+  if (p.longest_first) {
+    // Longest first: CTAs are dispatched in grid order, so grid z = r takes
+    // the sequence of rank r in decreasing length (ties by index) and the
+    // shortest work is left for the tail.  The lengths sit in the stage
+    // area, unused until the barrier after the query load.
+    __shared__ int pick[2];
+    int* lens = reinterpret_cast<int*>(base);
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) lens[i] = p.seq_lens[i];
+    __syncthreads();
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+      const int li = lens[i];
+      int r = 0;
+      for (int u = 0; u < p.num_seqs; ++u) {
+        const int lu = lens[u];
+        r += (lu > li) || (lu == li && u < i);
+      }
+      if (r == (int)blockIdx.z) {
+        pick[0] = i;
+        pick[1] = li;
+      }
+    }
+    __syncthreads();
+    s = pick[0];
+    L = pick[1];
+  } else {
+    L = p.seq_lens[s];
+  }
   const int P = p.partition_tokens;
   const bool split = P > 0;
   const int nparts = L <= 0 ? 0 : (split ? (L + P - 1) / P : 1);
@@ -161,9 +193,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const int n_stages = (tok1 - tok0 + kStageTokens - 1) / kStageTokens;
   const int NS = p.num_stages;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(base);
   float* q_s = reinterpret_cast<float*>(base + p.stage_area);
   float* p_all = q_s + G * D;

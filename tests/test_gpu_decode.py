@@ -202,10 +202,32 @@ def test_large_batch_without_the_length_cache():
     check(case, partitions=(0, 64))
 
 
+@pytest.mark.parametrize("n", [128, 129])
+def test_longest_first_ranks_every_sequence(n):
+    # The CUDA-core kernel takes batches of up to 128 sequences in decreasing
+    # length order: many equal lengths (ties broken by index), empty
+    # sequences and one long one must each land on exactly one grid slot;
+    # 129 sequences take the unranked order.
+    rng = np.random.default_rng(n)
+    lens = [int(x) for x in rng.choice([0, 1, 5, 16, 17, 40], size=n)]
+    lens[n // 2] = 700
+    case = workloads.custom(n, 4, 4, 128, 16, lens, "bf16", seed=n + 1, cache_fill="garbage")
+    ref, cache_ref = oracle_reference(case)
+    for p in (0, 64, -1):
+        dc = DeviceCase(case)
+        out = dc.step(p, kernel=pa.PA_KERNEL_SIMT)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
+        assert_close(to_f64(out), ref, case.dtype, "%d sequences partition=%d" % (n, p))
+
+
 def test_automatic_partition_choices():
     # Tensor-core path: no split when pairs give 4+ items per CTA and no
     # sequence is long, else the balanced split (long items beyond 256
-    # sequences); CUDA-core path: 512 halved toward 64.
+    # sequences); CUDA-core path: no split for batches it takes longest first
+    # with pairs for 4 CTAs per SM and lengths up to 2048, else 512 halved
+    # toward 64.
     cache = torch.zeros((2, 4, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     B = pa.PA_PARTITION_BALANCED
@@ -217,7 +239,13 @@ def test_automatic_partition_choices():
     c128 = torch.zeros((2, 4, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
     assert pa.pa_decode_partition_size(c128, 8, 32, 32768, -1) == B         # long context
     mha = torch.zeros((2, 4, 16, 40, 128), dtype=torch.bfloat16, device="cuda")
-    assert pa.pa_decode_partition_size(mha, 32, 40, 2048, -1) == 512        # CUDA cores, G = 1
+    assert pa.pa_decode_partition_size(mha, 32, 40, 2048, -1) == 0          # CUDA cores, G = 1
+    assert pa.pa_decode_partition_size(mha, 32, 40, 2049, -1) == 512        # a longer sequence
+    assert pa.pa_decode_partition_size(mha, 129, 40, 2048, -1) == 512       # not ranked
+    f32 = torch.zeros((2, 4, 16, 8, 128), dtype=torch.float32, device="cuda")
+    few = -(-4 * sms // 8) - 1                                               # pairs < 4 per SM
+    assert pa.pa_decode_partition_size(f32, few + 1, 8, 2048, -1) == 0
+    assert pa.pa_decode_partition_size(f32, few, 8, 2048, -1) > 0
 
 
 def test_balanced_split_applies_to_the_tensor_core_kernel_only():
@@ -231,7 +259,8 @@ def test_balanced_split_applies_to_the_tensor_core_kernel_only():
     assert pa.pa_decode_partition_size(cache, 257, 14, 2011, B) == \
         pa.pa_decode_partition_size(cache, 257, 14, 2011, -1)
     mha = torch.zeros((2, 4, 16, 40, 128), dtype=torch.bfloat16, device="cuda")
-    assert pa.pa_decode_partition_size(mha, 32, 40, 2048, B) == 512
+    assert pa.pa_decode_partition_size(mha, 32, 40, 2048, B) == 0
+    assert pa.pa_decode_partition_size(mha, 32, 40, 4096, B) == 512
     f32 = torch.zeros((2, 4, 16, 2, 64), dtype=torch.float32, device="cuda")
     assert pa.pa_decode_partition_size(f32, 64, 14, 2011, B) == \
         pa.pa_decode_partition_size(f32, 64, 14, 2011, -1)
