@@ -889,16 +889,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         const int nvalid = min(kTcTokens, it.tok1 - (it.tok0 + k * kTcTokens));
         const bool valid = row < nvalid;
-        if (!valid) {
-          // A stale row of V (past the sequence, or never loaded) must not
-          // reach the PV product: 0 * NaN would.
-          const uint32_t vrow = sbase + (uint32_t)slot * (uint32_t)lay.stage +
-                                (uint32_t)((row >> 3) * kChunkBytes + 1024 + (row & 7) * 128);
+        if (nvalid < kTcTokens) {
+          // Stale rows of V (past the sequence, or never loaded) must not
+          // reach the PV product: 0 * NaN would.  The rows of the ragged
+          // 8-token chunk are cleared one per thread; the whole chunks after
+          // it by the warpgroup in consecutive 16-byte pieces (a row per
+          // thread would put eight threads on the same banks).
+          const uint32_t vst = sbase + (uint32_t)slot * (uint32_t)lay.stage + 1024u;
+          const int clear0 = (nvalid + 7) >> 3;  // the first chunk with no valid row
+          if (!valid && row < clear0 * 8) {
+            const uint32_t vrow = vst + (uint32_t)((row >> 3) * kChunkBytes + (row & 7) * 128);
 #pragma unroll
-          for (int g = 0; g < kGroups; ++g)
+            for (int g = 0; g < kGroups; ++g)
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              st_shared_zero16(vrow + (uint32_t)(g * 2048 + c * 16));
+              for (int c = 0; c < 8; ++c)
+                st_shared_zero16(vrow + (uint32_t)(g * 2048 + c * 16));
+          }
+          const int pieces = (kTcTokens / 8 - clear0) * kGroups * 64;
+          for (int i = row; i < pieces; i += 128) {
+            const int ch = clear0 + i / (kGroups * 64);
+            const int rem = i % (kGroups * 64);
+            st_shared_zero16(vst + (uint32_t)(ch * kChunkBytes + (rem >> 6) * 2048 + (rem & 63) * 16));
+          }
         }
         float x[GP];
 #pragma unroll
