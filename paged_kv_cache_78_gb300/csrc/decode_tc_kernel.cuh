@@ -978,21 +978,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
       }
-      if (!ok) break;
-      // The item's last PV tile; decided by the whole warpgroup so that every
-      // warp executes the tensor-memory load convergently or not at all.
-      if (!(ok = softmax_group_all(ok && !flags[0]))) break;
-      ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, o_acc, alpha_prev);
-      if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
-      gk += n;
-
-      // l over the warpgroup's 128 token rows, then the item's output.
+      // A failed wait above is per thread: the barrier below settles it for
+      // the warpgroup (a thread leaving alone would strand the others).
+      // l over the warpgroup's 128 token rows (final after the last stage's
+      // weights, so it is summed while the last P.V runs), then the item's
+      // last PV tile; the barrier also decides for the whole warpgroup, so
+      // that every warp executes the tensor-memory load convergently or not
+      // at all.
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
         const float s_ = warp_sum(l_run[g]);
         if (lane == 0) red2[q4 * kTcHeads + g] = s_;
       }
       if (!(ok = softmax_group_all(ok && !flags[0]))) break;
+      ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, o_acc, alpha_prev);
+      if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
+      gk += n;
       {
         // One warp runs this once per item, so its instruction count is its
         // latency: per-head work (the sum over the four quarters, the
