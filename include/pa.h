@@ -45,7 +45,7 @@ extern "C" {
 typedef enum pa_status {
   PA_OK = 0,
   PA_ERR_INVALID_ARG = 1,    /* null pointer, bad size or inconsistent shape */
-  PA_ERR_UNSUPPORTED = 2,    /* valid, but no kernel in this build (head size, group) */
+  PA_ERR_UNSUPPORTED = 2,    /* valid, but the library has no kernel for it (head size, group) */
   PA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
   PA_ERR_OUT_OF_BLOCKS = 4,  /* block pool exhausted; pool state unchanged */
   PA_ERR_BAD_STATE = 5,      /* unknown sequence id, or an operation the state forbids */
