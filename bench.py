@@ -806,7 +806,7 @@ def main():
                 "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": (st.launches - (1 if args.fused else 0)) * args.steps,
         "roofline": {
-            "kernel": "pa_decode (%s%s)" % (st.kernel_name, " + lse_reduce_kernel" if st.partition else ""),
+            "kernel": "pa_decode (%s%s)" % (st.kernel_name, " + the log-sum-exp reduce" if st.partition else ""),
             "timed": "the decode call alone, %d launches after the timed steps, L2 evicted "
                      "before each" % args.steps,
             "bound": "hbm",
