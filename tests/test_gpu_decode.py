@@ -222,6 +222,29 @@ def test_longest_first_ranks_every_sequence(n):
         assert_close(to_f64(out), ref, case.dtype, "%d sequences partition=%d" % (n, p))
 
 
+@pytest.mark.parametrize("hq,hkv,d,fused", [(32, 8, 128, False), (32, 8, 128, True),
+                                            (14, 2, 64, False), (14, 2, 64, True)])
+def test_balanced_ranges_longer_than_the_stage_ring(hq, hkv, d, fused):
+    # Enough stages that every balanced range holds more than the three the
+    # ring keeps in flight (the first stage past the ring is prefetched into
+    # L2), with ragged ends, garbage in stale slots, and the newest token
+    # written by the decode itself in the fused form.
+    rng = np.random.default_rng(hq + d)
+    n = 8 if d == 128 else 64
+    lens = [int(x) for x in rng.integers(700, 2100, size=n)]
+    lens[1] = 1
+    case = workloads.custom(n, hq, hkv, d, 16, lens, "bf16", seed=hq * d + 5, cache_fill="garbage")
+    ref, cache_ref = oracle_reference(case)
+    dc = DeviceCase(case)
+    B = pa.PA_PARTITION_BALANCED
+    out = (dc.step_fused(B, kernel=pa.PA_KERNEL_TENSOR) if fused
+           else dc.step(B, kernel=pa.PA_KERNEL_TENSOR))
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert np.array_equal(bits(to_host_bits(dc.cache)), bits(cache_ref)), "cache differs"
+    assert_close(to_f64(out), ref, case.dtype, "balanced, long ranges, fused=%s" % fused)
+
+
 def test_automatic_partition_choices():
     # Tensor-core path: no split when pairs give 4+ items per CTA and no
     # sequence is long, else the balanced split (long items beyond 256
