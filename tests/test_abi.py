@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_cache_78_gb300 as pa
 
@@ -111,3 +112,20 @@ def test_zero_work_calls_are_noops():
     d = desc()
     assert pa.lib.pa_reshape_and_cache(None, ctypes.byref(d), None, None, None, 0, None) == pa.PA_OK
     assert pa.lib.pa_copy_blocks(None, ctypes.byref(d), None, 0, None) == pa.PA_OK
+
+
+def test_copy_bytes_argument_checks():
+    # Validated before any CUDA call: zero bytes is a no-op, null pointers
+    # and sizes past 2^40 are refused; the Python wrapper refuses tensors of
+    # different byte sizes and host tensors that are not page-locked.
+    assert pa.lib.pa_copy_bytes(None, None, 0, None) == pa.PA_OK
+    assert pa.lib.pa_copy_bytes(None, ctypes.c_void_p(64), 16, None) == pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_copy_bytes(ctypes.c_void_p(64), None, 16, None) == pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_copy_bytes(ctypes.c_void_p(64), ctypes.c_void_p(128), (1 << 40) + 1,
+                                None) == pa.PA_ERR_INVALID_ARG
+    a = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        pa.pa_copy_bytes(a, torch.zeros(8, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        pa.pa_copy_bytes(a, torch.zeros(16, dtype=torch.uint8))   # pageable host memory
+    pa.pa_copy_bytes(a[:0], a[:0])                                 # nothing to copy
