@@ -200,9 +200,10 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, partition: int):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary, when it was taken on the current kernel source."""
+    summary, when it was taken on the current kernel source and at the same
+    resolved partition (another split is another kernel variant)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -211,6 +212,8 @@ def ncu_traffic(workload: str):
         return None
     entry = data.get(workload)
     if not entry or entry.get("kernel_digest") != kernel_source_digest():
+        return None
+    if entry.get("partition") != partition:
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -816,7 +819,7 @@ def main():
             "unit": "GB/s",
             "frac": round(decode_gbs / peak, 4),
             "us_per_launch": round(r["decode_ms"] * 1e3, 2),
-            "traffic": ncu_traffic(args.workload),
+            "traffic": ncu_traffic(args.workload, st.partition),
         },
         "e2e": e2e,
         "paging": r["paging"],
