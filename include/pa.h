@@ -59,7 +59,7 @@ typedef enum pa_dtype { PA_BF16 = 0, PA_FP32 = 1 } pa_dtype;
 #define PA_DEVERR_SLOT 0x1u        /* reshape_and_cache: slot >= num_blocks * block_size */
 #define PA_DEVERR_BLOCK_ID 0x2u    /* decode / copy_blocks: block id outside [0, num_blocks) */
 #define PA_DEVERR_SEQ_LEN 0x4u     /* decode: seq_len > max_seq_len or > table capacity */
-#define PA_DEVERR_TIMEOUT 0x8u     /* a pipeline wait exceeded its limit (about 2 s) */
+#define PA_DEVERR_TIMEOUT 0x8u     /* a pipeline wait exceeded its limit (about 2 s by default) */
 
 /* partition_size of pa_decode: the stage-balanced split (see pa_decode). */
 #define PA_PARTITION_BALANCED (-2)
@@ -104,7 +104,8 @@ pa_status pa_reshape_and_cache(void* cache, const pa_cache_desc* desc, const voi
  *           no destination may also be a source in the same call (the pool
  *           only emits fresh destinations).  An id outside the pool skips the
  *           pair and records PA_DEVERR_BLOCK_ID.
- * num_pairs == 0 is a no-op.
+ * num_pairs == 0 is a no-op; num_pairs above 2^30 - 1 returns
+ * PA_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------- */
 pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* pairs,
                          int32_t num_pairs, void* stream);
@@ -122,7 +123,8 @@ pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* 
  * page-locked host memory; pageable host memory returns PA_ERR_INVALID_ARG
  * and launches nothing.  pairs: int64 [num_pairs][2] (pa_pool_swap_out /
  * pa_pool_swap_in give them).  An id outside its pool skips the pair and
- * records PA_DEVERR_BLOCK_ID.  Asynchronous on `stream`: the host pool may
+ * records PA_DEVERR_BLOCK_ID.  num_pairs above 2^30 - 1 returns
+ * PA_ERR_INVALID_ARG.  Asynchronous on `stream`: the host pool may
  * be reused only after the stream has passed the copy.
  * ------------------------------------------------------------------------- */
 pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const void* src_cache,
@@ -477,6 +479,22 @@ const char* pa_status_string(pa_status status);
  * turns tracing off (the default).  Host-side setting shared by all threads
  * of the process. */
 pa_status pa_set_decode_trace(void* device_buffer, size_t bytes, int32_t events_per_role);
+
+/* Limit, in SM clock cycles, of every pipeline wait of the tensor-core decode
+ * (a wait for a K/V stage, a score or output tile, a work-item slot or a free
+ * buffer; the MMA issuer's wait for any of its inputs).  A wait that runs
+ * out records PA_DEVERR_TIMEOUT; the CTA then stops taking work, waits for
+ * its own TMA loads and MMAs in flight (those waits keep the default limit,
+ * so nothing is left writing into memory the CTA gives back), frees its
+ * tensor memory and returns, and the rows of the call's output are
+ * undefined.  The work counters in the workspace header are left at zero,
+ * so the next call with the same workspace runs normally.  0 restores the
+ * default (4e9 cycles, about 2 s at 2 GHz; far beyond any healthy wait), a
+ * negative value returns PA_ERR_INVALID_ARG.  The pages have no counterpart:
+ * this is a test hook, which makes the timeout path run on purpose with a
+ * limit of a few cycles.  Host-side setting shared by all threads of the
+ * process; the CUDA-core kernel always keeps the default. */
+pa_status pa_set_decode_wait_limit(int64_t cycles);
 /* Library version, e.g. "0.1.0". */
 const char* pa_version(void);
 

@@ -50,6 +50,7 @@ EXPORTS = (
     "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache", "pa_pool_usage",
     "pa_swap_blocks", "pa_pool_set_cpu_blocks", "pa_pool_swap_out", "pa_pool_swap_in",
     "pa_pool_is_swapped", "pa_pool_num_free_cpu", "pa_decode_append", "pa_copy_bytes",
+    "pa_set_decode_wait_limit",
 )
 
 
@@ -102,6 +103,7 @@ def _load() -> ctypes.CDLL:
         "pa_pool_ref_count": [vp, i32, p_i32],
         "pa_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
         "pa_set_decode_trace": [vp, sz, i32],
+        "pa_set_decode_wait_limit": [i64],
         "pa_pool_add_seq_tokens": [vp, vp, i64, p_i64, p_i64],
         "pa_pool_append_token_id": [vp, i64, i32, p_i64, vp],
         "pa_pool_is_cached": [vp, i32, p_i32],
@@ -589,3 +591,9 @@ def pa_set_decode_trace(buffer: torch.Tensor | None, events_per_role: int = 0) -
     _check(lib.pa_set_decode_trace(_dev_ptr(buffer, "buffer"),
                                    buffer.numel() * buffer.element_size(), int(events_per_role)),
            "pa_set_decode_trace")
+
+
+def pa_set_decode_wait_limit(cycles: int) -> None:
+    """Limit (SM clock cycles) of the tensor-core decode's pipeline waits;
+    0 restores the default.  A test hook: see include/pa.h."""
+    _check(lib.pa_set_decode_wait_limit(int(cycles)), "pa_set_decode_wait_limit")

@@ -30,6 +30,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kStageBudgetBytes = 48 * 1024;
 constexpr int kStageBudgetWideBytes = 96 * 1024;
 constexpr int kMaxSmemPerCta = 227 * 1024;
+// Block copies launch two CTAs per pair along grid x, whose limit is 2^31 - 1.
+constexpr int32_t kMaxCopyPairs = (1 << 30) - 1;
 
 std::mutex g_mutex;
 unsigned int* g_error_word[kMaxDevices] = {};
@@ -45,6 +47,10 @@ EncodeTiledFn g_encode = nullptr;
 std::atomic<void*> g_trace_buf{nullptr};
 std::atomic<size_t> g_trace_bytes{0};
 std::atomic<int> g_trace_per_role{0};
+
+// Limit of the tensor-core decode's pipeline waits (pa_set_decode_wait_limit);
+// 0 = the default, kWaitLimitCycles.
+std::atomic<long long> g_wait_limit{0};
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 int ilog2(int x) {
@@ -259,6 +265,12 @@ pa_status pa_set_decode_trace(void* device_buffer, size_t bytes, int32_t events_
   return PA_OK;
 }
 
+pa_status pa_set_decode_wait_limit(int64_t cycles) {
+  if (cycles < 0) return PA_ERR_INVALID_ARG;
+  g_wait_limit.store(cycles);
+  return PA_OK;
+}
+
 const char* pa_status_string(pa_status s) {
   switch (s) {
     case PA_OK: return "ok";
@@ -314,7 +326,7 @@ pa_status pa_copy_blocks(void* cache, const pa_cache_desc* desc, const int64_t* 
                          int32_t num_pairs, void* stream) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
-  if (num_pairs < 0 || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
+  if (num_pairs < 0 || num_pairs > kMaxCopyPairs) return PA_ERR_INVALID_ARG;
   if (num_pairs == 0) return PA_OK;
   if (!cache || !pairs || !aligned(cache, 16) || !aligned(pairs, 8)) return PA_ERR_INVALID_ARG;
   unsigned int* err = nullptr;
@@ -356,7 +368,7 @@ pa_status pa_swap_blocks(void* dst_cache, const pa_cache_desc* dst_desc, const v
       dst_desc->num_kv_heads != src_desc->num_kv_heads ||
       dst_desc->head_size != src_desc->head_size || dst_desc->dtype != src_desc->dtype)
     return PA_ERR_INVALID_ARG;
-  if (num_pairs < 0 || num_pairs > (1 << 30)) return PA_ERR_INVALID_ARG;
+  if (num_pairs < 0 || num_pairs > kMaxCopyPairs) return PA_ERR_INVALID_ARG;
   if (num_pairs == 0) return PA_OK;
   if (!dst_cache || !src_cache || !pairs || !aligned(dst_cache, 16) || !aligned(src_cache, 16) ||
       !aligned(pairs, 8))
@@ -540,6 +552,8 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     prm.trace = static_cast<unsigned long long*>(g_trace_buf.load());
     prm.trace_per_role = g_trace_per_role.load();
     prm.trace_bytes = g_trace_bytes.load();
+    const long long limit = g_wait_limit.load();
+    prm.wait_limit = limit > 0 ? limit : pa::kWaitLimitCycles;
     prm.total_items = (int)std::min<long long>((long long)num_seqs * desc->num_kv_heads * max_parts,
                                                (1ll << 31) - 1);
     // With many partitions per sequence most (partition, sequence, head)

@@ -88,6 +88,7 @@ struct DecodeParams {
   int num_stages;        // a multiple of num_consumers
   int num_consumers;     // consumer warps that take stages (1..kConsumerWarps)
   int stage_area;        // bytes before the query buffer (stages, or the merge overlay)
+  long long wait_limit;  // tensor-core kernel: SM cycles a pipeline wait may take
 };
 
 // Dynamic shared memory a decode launch needs (the kernel aligns its base to 1024).

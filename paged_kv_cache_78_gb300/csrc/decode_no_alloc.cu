@@ -52,12 +52,15 @@ extern "C" pa_status pa_decode_no_alloc(void* out, const void* query, const void
                                           &need);
   if (st != PA_OK) return st;
   if (need > (size_t)PA_NO_ALLOC_WORKSPACE_BYTES) return PA_ERR_INVALID_ARG;
+  // Every call passes the array: even without a split, the tensor-core
+  // kernel keeps its work counters in the array's first 256 bytes.
   void* ws = nullptr;
-  if (need > 0 && (st = workspace_address(&ws)) != PA_OK) return st;
-  // The array's first 256 bytes (the tensor-core kernel's work counter) must
-  // be zero before a call: static storage starts at zero and every call
-  // leaves them zero.  The partials after them need no initialisation.
+  if ((st = workspace_address(&ws)) != PA_OK) return st;
+  // Those 256 bytes must be zero before a call: static storage starts at
+  // zero and every call leaves them zero.  The partials after them need no
+  // initialisation; under the balanced split the piece counts are written
+  // for every (sequence, KV head) pair before the reduce reads them.
   return pa_decode(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                    num_heads, scale, max_seq_len, partition_size, ws,
-                   need > 0 ? (size_t)PA_NO_ALLOC_WORKSPACE_BYTES : 0, stream);
+                   (size_t)PA_NO_ALLOC_WORKSPACE_BYTES, stream);
 }

@@ -213,10 +213,10 @@ __device__ __forceinline__ unsigned long long global_timer() {
 // gk % 2) into the fp32 accumulator, rescaled by that stage's factor.
 template <int GP>
 __device__ __forceinline__ bool tc_epilogue(int gk, const TcBars& b, uint32_t t_o_lane,
-                                            unsigned int* err, float (&o_acc)[GP],
-                                            const float (&alpha)[GP]) {
+                                            unsigned int* err, long long limit,
+                                            float (&o_acc)[GP], const float (&alpha)[GP]) {
   const int sb = gk & 1;
-  const bool w = mbar_wait_bounded(b.o_full + 8u * sb, (gk >> 1) & 1, err);
+  const bool w = mbar_wait_bounded(b.o_full + 8u * sb, (gk >> 1) & 1, err, limit);
   __syncwarp();
   tc::fence_after_sync();
   float ot[GP];
@@ -414,7 +414,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ranges = p.total_items;
     const int bq = bal ? max(1, (int)((total + (unsigned)ranges - 1) / (unsigned)ranges)) : 1;
     const float inv_bq = 1.f / (float)bq;
-    if (kBal && total >= (1u << 24)) {
+    // Past that, every pair goes through the zero-stage pass below, which
+    // records a piece count of 0 for it: the reduce then leaves its rows
+    // alone instead of combining whatever partials an earlier call left.
+    const bool overflow = kBal && total >= (1u << 24);
+    if (overflow) {
       if (blockIdx.x == 0 && lane == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
       total = 0;
     }
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         } else if (zs < p.num_seqs) {
-          if (pre[zs + 1] == pre[zs]) {
+          if (pre[zs + 1] == pre[zs] || overflow) {
             // No stages: zero rows for length 0 (a length error leaves its
             // rows undefined); no partials either way.
             if (lane == 0) p.part_counts[zs * p.num_kv_heads + zh] = 0;
@@ -573,7 +577,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       if (lane == 0) {
         if (ii >= kTcItemRing)
-          ok = mbar_wait_bounded(bars.it_free + 8u * j, ((ii / kTcItemRing) - 1) & 1, p.err);
+          ok = mbar_wait_bounded(bars.it_free + 8u * j, ((ii / kTcItemRing) - 1) & 1, p.err,
+                                 p.wait_limit);
         if (ok) {
           ring[j].s = it.s;
           ring[j].h = it.h;
@@ -603,7 +608,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Query rows h*G .. h*G+15 of sequence s (rows past G are masked).
       const int qb = qi & 1;
       if (lane == 0) {
-        if (qi >= 2) ok = mbar_wait_bounded(bars.q_free + 8u * qb, ((qi >> 1) - 1) & 1, p.err);
+        if (qi >= 2)
+          ok = mbar_wait_bounded(bars.q_free + 8u * qb, ((qi >> 1) - 1) & 1, p.err, p.wait_limit);
         if (ok) {
           mbar_arrive_expect_tx(bars.q_full + 8u * qb, (uint32_t)kQTile);
           const int row0 = it.s * p.num_heads + it.h * G;
@@ -631,7 +637,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int k = 0; k < it.nstages; ++k, ++gk) {
         const int slot = gk % NS;
         if (gk >= NS) {
-          if (lane == 0) ok = mbar_wait_bounded(bars.empty0 + 8u * slot, ((gk / NS) - 1) & 1, p.err);
+          if (lane == 0)
+            ok = mbar_wait_bounded(bars.empty0 + 8u * slot, ((gk / NS) - 1) & 1, p.err,
+                                   p.wait_limit);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
@@ -812,7 +820,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else if (abort) {
         ok = false;
         break;
-      } else if (__any_sync(0xffffffffu, clock64() - t_idle > kWaitLimitCycles)) {
+      } else if (__any_sync(0xffffffffu, clock64() - t_idle > p.wait_limit)) {
         if (leader) record_error(p.err, PA_DEVERR_TIMEOUT);
         ok = false;
         break;
@@ -820,7 +828,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (!ok && leader) flags[0] = 1;
     // Every MMA the leader issued completes before the CTA may free its
-    // tensor memory.
+    // tensor memory (this wait and the TMA drains below keep the full limit,
+    // whatever limit the pipeline waits had).
     if (leader) {
       tc::mma_commit(bars.drain);
       mbar_wait_bounded(bars.drain, 0, p.err);
@@ -837,7 +846,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     for (int ii = 0;; ++ii) {
       const int j = ii % kTcItemRing;
-      const bool w = mbar_wait_bounded(bars.it_full + 8u * j, (ii / kTcItemRing) & 1, p.err);
+      const bool w =
+          mbar_wait_bounded(bars.it_full + 8u * j, (ii / kTcItemRing) & 1, p.err, p.wait_limit);
       TcItem it;
       it.s = ring[j].s;
       it.h = ring[j].h;
@@ -876,7 +886,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int g_k = gk + k;
         const int sb = g_k & 1;
         const int slot = g_k % NS;
-        const bool ws = mbar_wait_bounded(bars.s_full + 8u * sb, (g_k >> 1) & 1, p.err);
+        const bool ws = mbar_wait_bounded(bars.s_full + 8u * sb, (g_k >> 1) & 1, p.err,
+                                          p.wait_limit);
         if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 15, (uint32_t)g_k);
         __syncwarp();
         tc::fence_after_sync();
@@ -972,7 +983,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 6, (uint32_t)g_k);
         else if (lane == 0) tc_trace<kTrace>(p, warp, ntr, 19, (uint32_t)((warp << 16) | g_k));
         if (k >= 1) {
-          ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, o_acc, alpha_prev) && ok;
+          ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, p.wait_limit, o_acc, alpha_prev) &&
+               ok;
           if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(g_k - 1));
         }
 #pragma unroll
@@ -991,7 +1003,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) red2[q4 * kTcHeads + g] = s_;
       }
       if (!(ok = softmax_group_all(ok && !flags[0]))) break;
-      ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, o_acc, alpha_prev);
+      ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, p.wait_limit, o_acc, alpha_prev);
       if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
       gk += n;
       {

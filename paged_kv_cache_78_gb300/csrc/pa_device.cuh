@@ -98,14 +98,16 @@ __device__ __forceinline__ void mbar_suspend(uint32_t bar, uint32_t parity, uint
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and records PA_DEVERR_TIMEOUT) if that takes longer than kWaitLimitCycles.
+// (and records PA_DEVERR_TIMEOUT) if that takes longer than `limit` SM clock
+// cycles (kWaitLimitCycles unless the launch asked for another limit).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  unsigned int* err) {
+                                                  unsigned int* err,
+                                                  long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && clock64() - t0 > kWaitLimitCycles) {
+    if ((i & 63u) == 0 && clock64() - t0 > limit) {
       record_error(err, PA_DEVERR_TIMEOUT);
       return false;
     }

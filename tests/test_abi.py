@@ -114,6 +114,23 @@ def test_zero_work_calls_are_noops():
     assert pa.lib.pa_copy_blocks(None, ctypes.byref(d), None, 0, None) == pa.PA_OK
 
 
+def test_copy_pair_count_limit():
+    # Two CTAs per pair along grid x: more than 2^30 - 1 pairs is refused
+    # before any CUDA call.
+    d = desc()
+    p = ctypes.c_void_p(256)
+    assert pa.lib.pa_copy_blocks(p, ctypes.byref(d), p, 1 << 30, None) == pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_swap_blocks(p, ctypes.byref(d), p, ctypes.byref(d), p, 1 << 30,
+                                 None) == pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_copy_blocks(p, ctypes.byref(d), p, -1, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_wait_limit_argument_checks():
+    # A host-side setting: a negative limit is refused, 0 restores the default.
+    assert pa.lib.pa_set_decode_wait_limit(-1) == pa.PA_ERR_INVALID_ARG
+    assert pa.lib.pa_set_decode_wait_limit(0) == pa.PA_OK
+
+
 def test_copy_bytes_argument_checks():
     # Validated before any CUDA call: zero bytes is a no-op, null pointers
     # and sizes past 2^40 are refused; the Python wrapper refuses tensors of
