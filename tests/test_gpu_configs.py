@@ -53,12 +53,35 @@ def test_opt13b_mha_block_size_sweep(block_size):
     run_case(case, -1, sample)
 
 
-def test_long_context_uniform():
-    run_case(workloads.long_context(mixed=False), 512, [0, 5])
+@pytest.fixture(scope="module", params=[False, True], ids=["uniform_8x32768", "mixed_to_131072"])
+def long_context_case(request):
+    """The long-context batch on the device, with the oracle's cache and its
+    decode of every sequence (computed once for every partition mode)."""
+    case = workloads.long_context(mixed=request.param)
+    dc = DeviceCase(case)
+    cache_ref = oracle.fill_cache(case)
+    ref = oracle.decode(case.query, cache_ref, case.block_tables, case.seq_lens, case.scale)
+    return case, dc, cache_ref, ref
 
 
-def test_long_context_mixed():
-    run_case(workloads.long_context(mixed=True), 512, None)
+@pytest.mark.parametrize("fused", [False, True], ids=["write_then_decode", "fused_write"])
+@pytest.mark.parametrize("partition", [512, -1, pa.PA_PARTITION_BALANCED])
+def test_long_context_every_sequence(long_context_case, partition, fused):
+    # 512-token partitions (the workload's statement), the automatic choice
+    # and the balanced split (what -1 resolves to here), with the step's
+    # cache write as its own call or fused into the decode; every sequence of
+    # the batch against the oracle.
+    case, dc, cache_ref, ref = long_context_case
+    if partition == -1:
+        assert pa.pa_decode_partition_size(dc.cache, case.num_seqs, case.num_heads,
+                                           case.max_seq_len, -1) == pa.PA_PARTITION_BALANCED
+    dc.out.zero_()
+    out = dc.step_fused(partition) if fused else dc.step(partition)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert_close(to_f64(out), ref, case.dtype, "%s partition %d" % (case.name, partition))
+    if fused:
+        assert np.array_equal(to_host_bits(dc.cache), cache_ref), "cache differs from the oracle"
 
 
 def replay_script(script, num_heads, num_kv_heads, head_size, seed):
