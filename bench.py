@@ -5,18 +5,24 @@ new tokens (pa_reshape_and_cache through slot_mapping), any copy-on-write
 block copies, then paged decode attention (pa_decode: single pass, or
 split-KV partitions plus the log-sum-exp reduce).
 
-Default workload: the Qwen2-0.5B-shaped GQA batch (64 sequences, lengths
-U[128, 2048], 14 query / 2 KV heads of 64, block size 16, a pool of 16384
-blocks, 64 new tokens per step).  Other workloads: --workload.
+Default workload: the long-context batch (8 sequences of 32768 tokens, 32
+query / 8 KV heads of 128, block size 16, split-KV in 512-token partitions
+with the log-sum-exp reduce, one new token per sequence per step): the
+largest single-GPU configuration, and one of the two the >= 70 % of HBM
+bandwidth target names.  Other workloads (the Qwen2-0.5B-shaped GQA batch,
+the OPT-13B-shaped MHA batch at block sizes 8/16/32, the mixed-length
+long-context batch, the shared-prefix batches): --workload.
 
 Printed: one JSON line (rank 0).  `value` is algorithmic GB/s of the whole
 step (bytes the step must move, divided by its device time); `roofline`
 reports the decode call alone against the measured HBM copy bandwidth;
 `e2e` repeats the step through the C ABI with host buffers (pinned H2D of
 the step's inputs, D2H of the output) inside the timed region;
-`cpu_baseline` times the CPU oracle on this host.  L2 is flushed before every
-timed step: a 256 MB write, then a 256 MB read so that the written lines are
-evicted (and written back) before the step starts.
+`cpu_baseline` times the CPU oracle on this host, on all its cores and on
+one.  L2 is flushed before every timed step: a 256 MB write, then a 256 MB
+read so that the written lines are evicted (and written back) before the step
+starts.  Right before the timed steps the step runs untimed for a quarter of
+a second, so the first timed steps do not start from an idle clock.
 
 `--impl reference` times the CPU oracle as the reference arm, on the same
 workload, metric and unit.
@@ -45,6 +51,17 @@ import workloads  # noqa: E402
 METRIC = "paged decode attn: achieved HBM GB/s (% of GB300 peak), µs per batch step"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 256 << 20
+PREROLL_S = 0.25
+
+
+def spread_us(times_ms):
+    """Mean, median, min and max of per-launch event times, in µs."""
+    if not times_ms:
+        return None
+    return {"mean": round(sum(times_ms) / len(times_ms) * 1e3, 2),
+            "median": round(statistics.median(times_ms) * 1e3, 2),
+            "min": round(min(times_ms) * 1e3, 2), "max": round(max(times_ms) * 1e3, 2),
+            "first": round(times_ms[0] * 1e3, 2)}
 
 
 def make_workload(name: str):
@@ -461,6 +478,14 @@ def run_gpu(args, rank, world, device):
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    # Keep the GPU busy up to the timed region (the sleep above lets its
+    # clock fall to idle, and the first steps after an idle spell run slow).
+    t_pre = time.time()
+    while time.time() - t_pre < PREROLL_S:
+        for _ in range(8):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     ev = [mk() for _ in range(args.steps)]
     ev_dec = [mk() for _ in range(args.steps)]
@@ -486,10 +511,13 @@ def run_gpu(args, rank, world, device):
     t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = sum(a.elapsed_time(b) for a, b in ev)
-    decode_ms = sum(a.elapsed_time(b) for a, b in ev_dec)
+    step_each = [a.elapsed_time(b) for a, b in ev]
+    decode_each = [a.elapsed_time(b) for a, b in ev_dec]
+    step_ms = sum(step_each)
+    decode_ms = sum(decode_each)
     if world > 1:
         step_ms, decode_ms = max_over_ranks([step_ms, decode_ms], device)
+    spread = {"step_us": spread_us(step_each), "decode_us": spread_us(decode_each)}
 
     # Outside the timed steps: the decode call warm (no eviction, inputs left
     # in L2 by the previous call), and the same tokens in the unpaged layout
@@ -574,7 +602,7 @@ def run_gpu(args, rank, world, device):
             sampler.stop()
         return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
                 "decode_ms": decode_ms / args.steps, "e2e_ms": None, "clocks": clocks,
-                "h2d": h2d, "d2h": d2h, "paging": paging}
+                "h2d": h2d, "d2h": d2h, "paging": paging, "spread": spread}
     for _ in range(max(3, args.warmup // 4)):
         flush.zero_()
         e2e_step()
@@ -601,7 +629,9 @@ def run_gpu(args, rank, world, device):
         e2e_call()
         b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2) / e2e_steps
+    e2e_each = [a.elapsed_time(b) for a, b in ev2]
+    e2e_ms = sum(e2e_each) / e2e_steps
+    spread["e2e_us"] = spread_us(e2e_each)
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
@@ -610,7 +640,7 @@ def run_gpu(args, rank, world, device):
         e2e_ms = max_over_ranks([e2e_ms], device)[0]
     return {"case": case, "step": st, "bytes": nbytes, "step_ms": step_ms / args.steps,
             "decode_ms": decode_ms / args.steps, "e2e_ms": e2e_ms, "clocks": clocks,
-            "h2d": h2d, "d2h": d2h, "paging": paging}
+            "h2d": h2d, "d2h": d2h, "paging": paging, "spread": spread}
 
 
 # ---------------------------------------------------------------------------
@@ -660,17 +690,29 @@ def oracle_sample(case, per_step_s: float):
     return probe if n == 1 else OracleStep(case, min(n, case.num_seqs))
 
 
-def time_oracle(case, budget_s: float, steps: int = 0):
-    """Median-free list of per-step times: `steps` runs, or as many as fit budget_s."""
-    per_step = budget_s / max(1, steps) if steps else budget_s / 5
-    step = oracle_sample(case, per_step)
-    times = []
-    t_start = time.time()
-    while (steps and len(times) < steps) or (not steps and (not times or time.time() - t_start < budget_s)):
-        t = time.perf_counter()
-        step.run()
-        times.append(time.perf_counter() - t)
-    return times, step, step.oracle.num_threads()
+def time_oracle(case, budget_s: float, steps: int = 0, threads: int = 0):
+    """Per-step times of the oracle on a bounded sample of the batch: `steps`
+    runs, or as many as fit budget_s; on `threads` threads (0 = all of the
+    host's cores, the oracle's default).  Returns (times, sample, threads)."""
+    import oracle
+
+    every = oracle.num_threads()
+    if threads:
+        oracle.set_num_threads(threads)
+    try:
+        per_step = budget_s / max(1, steps) if steps else budget_s / 5
+        step = oracle_sample(case, per_step)
+        times = []
+        t_start = time.time()
+        while (steps and len(times) < steps) or \
+                (not steps and (not times or time.time() - t_start < budget_s)):
+            t = time.perf_counter()
+            step.run()
+            times.append(time.perf_counter() - t)
+        used = oracle.num_threads()
+    finally:
+        oracle.set_num_threads(every)
+    return times, step, used
 
 
 def config_for(case, name, partition=0):
@@ -693,7 +735,7 @@ def main():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen2_gqa")
+    ap.add_argument("--workload", default="long_context")
     ap.add_argument("--partition", type=int, default=-1,
                     help="tokens per split-KV partition; 0 = no split, -1 = library's choice")
     ap.add_argument("--graph", type=int, default=0,
@@ -774,14 +816,20 @@ def main():
 
     cpu = None
     if args.cpu_budget > 0:
-        times, ostep, cores = time_oracle(case, budget_s=args.cpu_budget)
-        cpu_sec = statistics.median(times)
-        cpu = {"value": round(ostep.bytes() / cpu_sec / 1e9, 4), "unit": "GB/s", "cores": cores,
-               "kind": "oracle",
-               "sample": "cache write of the new tokens and binary64 decode of the first %d of "
-                         "%d sequences, median of %d runs in %.0f s"
-                         % (ostep.n, case.num_seqs, len(times), sum(times)),
-               "ms_per_step": round(cpu_sec * 1e3, 2)}
+        def oracle_leg(threads):
+            times, ostep, cores = time_oracle(case, budget_s=args.cpu_budget, threads=threads)
+            sec = statistics.median(times)
+            return {"value": round(ostep.bytes() / sec / 1e9, 4), "unit": "GB/s", "cores": cores,
+                    "kind": "oracle",
+                    "sample": "cache write of the new tokens and binary64 decode of the first %d "
+                              "of %d sequences, median of %d runs in %.0f s"
+                              % (ostep.n, case.num_seqs, len(times), sum(times)),
+                    "ms_per_step": round(sec * 1e3, 2)}
+
+        # All of the host's cores (the oracle's OpenMP loop over sequences and
+        # query heads), then one core.
+        cpu = oracle_leg(0)
+        cpu["single_core"] = oracle_leg(1)
 
     line = {
         "metric": METRIC,
@@ -822,6 +870,7 @@ def main():
             "traffic": ncu_traffic(args.workload, st.partition),
         },
         "e2e": e2e,
+        "spread": r["spread"],
         "paging": r["paging"],
         "memory": memory_report(pa, case, args.workload),
         "clocks": r["clocks"],

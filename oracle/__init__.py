@@ -58,6 +58,8 @@ def bind(path: str):
     lib = ctypes.CDLL(path)
     p, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
     lib.oracle_num_threads.restype = i32
+    lib.oracle_set_num_threads.argtypes = [i32]
+    lib.oracle_set_num_threads.restype = None
     lib.oracle_reshape_and_cache.argtypes = [p, i64, i32, i32, i32, i32, p, p, p, i64]
     lib.oracle_reshape_and_cache.restype = i32
     lib.oracle_copy_blocks.argtypes = [p, i64, i32, i32, i32, i32, p, i64]
@@ -95,6 +97,11 @@ def dtype_code(arr: np.ndarray) -> int:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls from this thread (timing only)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def reshape_and_cache(cache: np.ndarray, key: np.ndarray, value: np.ndarray,

@@ -75,6 +75,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads of the calling thread's later parallel loops (n >= 1); timing
+ * only, the results do not depend on it. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /*
  * Write the new tokens' keys and values into the cache through slot_mapping:
  * cache[0][slot / bs][slot % bs][h][:] = key[t][h][:] and the same for value

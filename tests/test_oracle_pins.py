@@ -228,6 +228,24 @@ def test_decode_block_relabelling_is_bit_identical():
     assert np.array_equal(got, ref)
 
 
+def test_decode_does_not_depend_on_the_thread_count():
+    # The baseline times the oracle on every core and on one; each (sequence,
+    # query head) row is computed by one thread in a fixed order, so both
+    # give the same bits.
+    case = workloads.custom(4, 8, 2, 64, 8, [5, 40, 64, 77], "bf16", seed=19)
+    cache = oracle.fill_cache(case)
+    ref = oracle.decode(case.query, cache, case.block_tables, case.seq_lens, case.scale)
+    every = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        assert oracle.num_threads() == 1
+        got = oracle.decode(case.query, cache, case.block_tables, case.seq_lens, case.scale)
+    finally:
+        oracle.set_num_threads(every)
+    assert oracle.num_threads() == every
+    assert np.array_equal(got, ref)
+
+
 def test_unpaged_layout_of_the_same_tokens_gives_the_same_output():
     # The bench's paging-overhead run: consecutive physical blocks are one more
     # relabelling of the same tokens.
