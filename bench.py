@@ -151,11 +151,14 @@ def memory_report(pa, case, workload: str) -> dict:
 BALANCED = -2  # the library's PA_PARTITION_BALANCED
 
 
-def balanced_pieces(case, ranges: int) -> np.ndarray:
+def balanced_pieces(case, ranges: int, start=None) -> np.ndarray:
     """Pieces of each (sequence, KV head) pair under the balanced split: the
-    pairs' 128-token stages laid end to end, cut every ceil(total / ranges)
-    stages."""
-    n = (case.seq_lens.astype(np.int64) + 127) // 128
+    pairs' 128-token stages (of tokens [start, L) when given) laid end to
+    end, cut every ceil(total / ranges) stages."""
+    lens = case.seq_lens.astype(np.int64)
+    if start is not None:
+        lens = np.where(lens > 0, lens - np.minimum(start, lens - 1), 0)
+    n = (lens + 127) // 128
     per_pair = np.repeat(n, case.num_kv_heads)
     total = int(per_pair.sum())
     q = max(1, -(-total // ranges))
@@ -164,12 +167,24 @@ def balanced_pieces(case, ranges: int) -> np.ndarray:
     return pieces
 
 
-def step_bytes(case, partition: int = 0, ranges: int = 0) -> dict:
+def shared_ranges(case, plan, sms: int) -> int:
+    """Stage ranges per (chunk, KV head) of the shared-prefix decode's group
+    kernel: the library's rule (fill the SMs, no more than the shortest
+    chunk's stages, at most 16)."""
+    units = plan.num_chunks * case.num_kv_heads
+    r = sms // units if units else 1
+    r = min(r, plan.info.min_chunk_stages, 16)
+    return max(1, r)
+
+
+def step_bytes(case, partition: int = 0, ranges: int = 0, plan=None, sms: int = 0) -> dict:
     """Algorithmic bytes of one step: what the operations must read and write
     once.  With split-KV partitions, each sequence of more than one partition
     also writes and reads its fp32 partials (head_size values and a log-sum-exp
     per query head and partition); the balanced split (over `ranges` stage
-    ranges) writes and reads those of every pair cut into several pieces."""
+    ranges) writes and reads those of every pair cut into several pieces; the
+    shared-prefix decode those of every member row (its shared ranges and its
+    own part)."""
     eb = workloads.elem_bytes(case.dtype)
     s, hq, hkv, d = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_size
     lens = case.seq_lens.astype(np.int64)
@@ -182,7 +197,18 @@ def step_bytes(case, partition: int = 0, ranges: int = 0) -> dict:
         kv = case.meta["unique_slots"] * hkv * d * 2 * eb
     decode = kv + 2 * s * hq * d * eb + 4 * blocks + 4 * s
     partials = 0
-    if partition > 0:
+    if plan is not None and plan.num_chunks:
+        # Member rows: one partial per range of the group kernel when it has
+        # several; the other sequences: the balanced split's pieces.
+        r = shared_ranges(case, plan, sms)
+        member = np.array(plan.seq_start(), dtype=np.int64) > 0
+        if r > 1:
+            partials += int(member.sum()) * hq * r * (d + 1) * 4 * 2
+        if not member.all():
+            pieces = balanced_pieces(case, sms * (2 if d == 64 else 1))
+            pieces = np.where(np.repeat(member, hkv), 0, pieces)
+            partials += int(pieces[pieces > 1].sum()) * (hq // hkv) * (d + 1) * 4 * 2
+    elif partition > 0:
         parts = (lens + partition - 1) // partition
         partials = int(parts[parts > 1].sum()) * hq * (d + 1) * 4 * 2
     elif partition == BALANCED:
@@ -305,11 +331,14 @@ def bf16_or_f32_to_device(torch, a, device):
 
 
 class GpuStep:
-    """A workload resident on the device, and its step through the C ABI."""
+    """A workload resident on the device, and its step through the C ABI.
+    With `shared`, the decode is pa_decode_shared over a plan of the blocks
+    the batch's sequences share (built on the host from the block tables)."""
 
-    def __init__(self, torch, pa, case, device, partition, kernel=0):
+    def __init__(self, torch, pa, case, device, partition, kernel=0, shared=False):
         self.torch, self.pa, self.case, self.device = torch, pa, case, device
         self.kernel = kernel
+        self.plan = None
         to_dev = lambda a: bf16_or_f32_to_device(torch, a, device)
         self.cache = to_dev(case.initial_cache())
         bt_host = torch.from_numpy(case.block_tables)
@@ -337,31 +366,57 @@ class GpuStep:
                                                      case.max_seq_len, partition)
         nbytes = pa.pa_decode_workspace_size(self.cache, case.num_seqs, case.num_heads,
                                              case.max_seq_len, self.partition)
-        self.ws = pa.alloc_workspace(nbytes, device)
         split = self.partition > 0 or (self.partition == BALANCED and case.max_seq_len > 128)
         self.launches = 2 + (1 if split else 0)
+        if shared:
+            self.plan = pa.SharedPlan(case.block_tables, case.seq_lens, case.block_size,
+                                      case.num_heads, case.num_kv_heads)
+            self.plan_dev = self.plan.upload(device)
+            nbytes = pa.pa_decode_shared_workspace_size(self.cache, case.num_seqs, case.num_heads,
+                                                        case.max_seq_len, self.plan)
+            sms = torch.cuda.get_device_properties(device).multi_processor_count
+            others = self.plan.info.num_members < case.num_seqs
+            self.launches = 1 + (1 + int(others) + int(others or shared_ranges(
+                case, self.plan, sms) > 1) if self.plan.num_chunks else 1)
+        self.ws = pa.alloc_workspace(nbytes, device)
         if int((case.seq_lens > 0).sum()) != case.num_seqs:
             raise SystemExit("the bench's workloads give every sequence a new token")
         family = pa.pa_decode_select_kernel(self.cache, case.num_seqs, case.num_heads,
                                             self.q.data_ptr(), kernel)
         self.kernel_name = ("paged_decode_tc_kernel" if family == pa.PA_KERNEL_TENSOR
                             else "paged_decode_kernel")
+        if self.plan is not None:
+            self.kernel_name = "paged_decode_shared_kernel + paged_decode_tc_kernel"
 
     def write(self):
         self.pa.pa_reshape_and_cache(self.cache, self.k, self.v, self.slots)
 
     def decode(self):
         c = self.case
+        if self.plan is not None:
+            self.pa.pa_decode_shared(self.out, self.q, self.cache, self.bt, self.sl, c.scale,
+                                     c.max_seq_len, self.plan, self.plan_dev, self.ws)
+            return
         self.pa.pa_decode(self.out, self.q, self.cache, self.bt, self.sl, c.scale, c.max_seq_len,
                           self.partition, self.ws, kernel=self.kernel)
 
     def write_and_decode(self):
         """The step as one call: the decode writes each sequence's newest
-        token itself (pa_decode_append)."""
+        token itself (pa_decode_append, or pa_decode_shared with the new
+        tokens)."""
         c = self.case
+        if self.plan is not None:
+            self.pa.pa_decode_shared(self.out, self.q, self.cache, self.bt, self.sl, c.scale,
+                                     c.max_seq_len, self.plan, self.plan_dev, self.ws, self.k,
+                                     self.v)
+            return
         self.pa.pa_decode_append(self.out, self.q, self.cache, self.bt, self.sl, c.scale,
                                  c.max_seq_len, self.k, self.v, self.partition, self.ws,
                                  kernel=self.kernel)
+
+    def inputs(self):
+        """Names of the step's host-supplied inputs (the plan too when shared)."""
+        return STEP_INPUTS + (("plan_dev",) if self.plan is not None else ())
 
 
 STEP_INPUTS = ("q", "k", "v", "slots", "bt", "sl")
@@ -373,13 +428,14 @@ def pack_step_inputs(torch, st, device):
     of the same bytes: a step's host-to-device traffic is then one copy.
     The step's tensors become views into the arena."""
     spans, off = {}, 0
-    for name in STEP_INPUTS:
+    names = st.inputs()
+    for name in names:
         t = getattr(st, name)
         nbytes = t.numel() * t.element_size()
         spans[name] = (off, nbytes)
         off += (nbytes + 255) // 256 * 256
     arena = torch.zeros(off, dtype=torch.uint8, device=device)
-    for name in STEP_INPUTS:
+    for name in names:
         t = getattr(st, name)
         o, nbytes = spans[name]
         view = arena[o:o + nbytes].view(t.dtype).view(t.shape)
@@ -387,6 +443,10 @@ def pack_step_inputs(torch, st, device):
         setattr(st, name, view)
     host = arena.cpu().pin_memory()
     return arena, host
+
+
+def sms_of(torch, device) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
 
 
 def max_over_ranks(values, device):
@@ -408,10 +468,12 @@ def run_gpu(args, rank, world, device):
     torch.cuda.set_device(device)
     case = make_workload(args.workload)
     partition = args.partition if args.partition != -1 else WORKLOAD_PARTITION.get(args.workload, -1)
-    st = GpuStep(torch, pa, case, device, partition, args.kernel)
+    shared = args.shared == 1 or (args.shared == -1 and args.workload.startswith("shared_prefix"))
+    st = GpuStep(torch, pa, case, device, partition, args.kernel, shared)
     arena, arena_host = pack_step_inputs(torch, st, device)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    nbytes = step_bytes(case, st.partition, ranges=sms * (2 if case.head_size == 64 else 1))
+    nbytes = step_bytes(case, st.partition, ranges=sms * (2 if case.head_size == 64 else 1),
+                        plan=st.plan, sms=sms)
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -753,6 +815,10 @@ def main():
     ap.add_argument("--fused", type=int, default=1,
                     help="1: the step is one pa_decode_append (the decode writes the new tokens); "
                          "0: pa_reshape_and_cache, then pa_decode")
+    ap.add_argument("--shared", type=int, default=-1,
+                    help="1: decode with pa_decode_shared (blocks the sequences share attended "
+                         "once per group), 0: pa_decode; -1 (default): 1 for the shared-prefix "
+                         "workloads")
     ap.add_argument("--paging", type=int, default=1,
                     help="also time the decode warm and on the unpaged (consecutive-block) layout")
     args = ap.parse_args()
@@ -847,8 +913,15 @@ def main():
         "data": "synthetic",
         "config": config_for(case, args.workload, st.partition),
         "run": {"partition_size": st.partition, "cuda_graph": bool(args.graph),
-                "step_calls": "pa_decode_append" if args.fused else
-                              "pa_reshape_and_cache + pa_decode",
+                "step_calls": ("pa_decode_shared (new tokens written by the decode)"
+                               if st.plan is not None and args.fused else
+                               "pa_reshape_and_cache + pa_decode_shared" if st.plan is not None
+                               else "pa_decode_append" if args.fused else
+                               "pa_reshape_and_cache + pa_decode"),
+                "shared_plan": None if st.plan is None else {
+                    "chunks": st.plan.num_chunks, "members": st.plan.info.num_members,
+                    "min_shared_tokens": st.plan.info.min_shared_tokens,
+                    "ranges": shared_ranges(case, st.plan, sms_of(torch, st.device))},
                 "decode_kernel": {0: "auto", 1: "cuda cores", 2: "tensor cores"}[args.kernel] +
                                  " -> " + st.kernel_name,
                 "decode_bytes": nbytes["decode"],
@@ -857,7 +930,11 @@ def main():
                 "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": (st.launches - (1 if args.fused else 0)) * args.steps,
         "roofline": {
-            "kernel": "pa_decode (%s%s)" % (st.kernel_name, " + the log-sum-exp reduce" if st.partition else ""),
+            "kernel": "%s (%s%s)" % ("pa_decode_shared" if st.plan is not None else "pa_decode",
+                                     st.kernel_name,
+                                     " + the log-sum-exp reduce"
+                                     if st.partition or (st.plan is not None and
+                                                         st.plan.num_chunks) else ""),
             "timed": "the decode call alone, %d launches after the timed steps, L2 evicted "
                      "before each" % args.steps,
             "bound": "hbm",
@@ -867,7 +944,8 @@ def main():
             "unit": "GB/s",
             "frac": round(decode_gbs / peak, 4),
             "us_per_launch": round(r["decode_ms"] * 1e3, 2),
-            "traffic": ncu_traffic(args.workload, st.partition),
+            "traffic": ncu_traffic(args.workload + ("_shared" if st.plan is not None else ""),
+                                   st.partition),
         },
         "e2e": e2e,
         "spread": r["spread"],

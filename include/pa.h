@@ -245,6 +245,85 @@ pa_status pa_decode_append(void* out, const void* query, void* cache, const pa_c
                            const void* key_new, const void* value_new, void* workspace,
                            size_t workspace_bytes, int32_t kernel, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Shared-prefix decode.  Sequences that share leading physical blocks
+ * (parallel samples forked from one prompt, studying-code.tistory.com/16,
+ * section "생성 단계에서의 Copy-on-Write", tech.blogsailing.com/?p=100,
+ * section 3; requests whose prompts hit the same cached prefix, itan.pw page,
+ * section "プレイフィックスキャッシュの詳細") hold the same K/V rows for those
+ * tokens.  The pages share the memory; these calls also share the work: a
+ * group's query rows (up to 128 per tile) attend the shared blocks together,
+ * each block read once, and then their members' own blocks, packed several
+ * members to a 128-token stage with every row masked to its own member's
+ * tokens; the result is the same as pa_decode's.  Sequences outside every
+ * group go to the tensor-core decode in the same call.
+ *
+ * pa_decode_shared_plan (host only) finds the sharing from the host copy of
+ * the block tables: sequences with the same first block id form a group;
+ * its shared length is the longest run of leading block ids all members
+ * have in common, capped for every member at floor((seq_len - 1) /
+ * block_size) blocks (each member's newest token stays its own).  Groups of
+ * one member or of fewer than min_shared_blocks shared blocks are dropped.
+ * A group is cut into chunks of 4 * floor(32 / G) members (G = num_heads /
+ * num_kv_heads; at most PA_SHARED_TILE_ROWS query rows, a member's G rows in
+ * one of four 32-row warps).  The plan is written to `plan` (host,
+ * PA_SHARED_PLAN_INTS(num_seqs) int32 at least), its sizes to *info:
+ *   plan[0..3]   chunks, sequences, members, G
+ *   then per chunk {first member index, members, shared tokens, group},
+ *   per sequence the first token of its own part (0 outside a group), and
+ *   the members' sequence ids.
+ * Returns PA_ERR_INVALID_ARG for bad sizes, a table too short for a length,
+ * or G > 32.
+ * ------------------------------------------------------------------------- */
+#define PA_SHARED_TILE_ROWS 128
+#define PA_SHARED_PLAN_INTS(num_seqs) (4 + 6 * (int64_t)(num_seqs))
+typedef struct pa_shared_plan_info {
+  int32_t num_chunks;         /* chunks of query rows (0: nothing is shared) */
+  int32_t num_members;        /* sequences in a group */
+  int32_t min_shared_tokens;  /* fewest shared tokens of any chunk */
+  int32_t min_chunk_stages;   /* fewest 128-token stages of any chunk (shared and own tokens) */
+  int32_t group_size;         /* G the plan was built for */
+  int32_t plan_ints;          /* int32 of the plan in use (the bytes to upload) */
+} pa_shared_plan_info;
+pa_status pa_decode_shared_plan(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, int32_t num_seqs, int32_t block_size,
+                                int32_t num_heads, int32_t num_kv_heads,
+                                int32_t min_shared_blocks, int32_t* plan, size_t plan_ints,
+                                pa_shared_plan_info* info);
+
+/* Workspace bytes of pa_decode_shared for this batch (max_seq_len bounds
+ * its lengths, as in pa_decode) and plan (256-byte aligned; zero it once at
+ * allocation, every call leaves its header zero). */
+pa_status pa_decode_shared_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
+                                          int32_t num_heads, int32_t max_seq_len,
+                                          const pa_shared_plan_info* info, size_t* bytes);
+
+/* pa_decode over the same arguments, with the shared blocks of the plan's
+ * groups attended once per group.  `plan` is a device copy of the first
+ * info->plan_ints int32 that pa_decode_shared_plan wrote for exactly these
+ * block tables and lengths (a plan for other tables gives wrong rows; it
+ * cannot make the kernels touch memory outside the pool, the tables, the
+ * queries, the workspace or the output: member ids, shared lengths and
+ * ranges are checked on the device, and a violation records
+ * PA_DEVERR_SEQ_LEN and leaves those rows undefined).  key_new / value_new:
+ * both NULL, or the step's newest tokens as in pa_decode_append (written into
+ * the cache by the decode).  The tensor-core decode must support the shape
+ * (bf16, head size 64 or 128, G <= 16, blocks of 8 tokens or more, a
+ * 16-byte aligned query), else PA_ERR_UNSUPPORTED.  A plan without chunks
+ * runs pa_decode_ex's unsplit tensor-core decode.  Asynchronous on `stream`.
+ * Launches: the group kernel (grid: stage ranges x KV heads x chunks, the
+ * ranges chosen to fill the SMs; with one range it writes final rows); the
+ * tensor-core decode of the sequences outside every group, if any (the
+ * balanced split for batches of up to 256 sequences); the log-sum-exp reduce
+ * when some row has several partials. */
+pa_status pa_decode_shared(void* out, const void* query, void* cache, const pa_cache_desc* desc,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                           float scale, int32_t max_seq_len, const int32_t* plan,
+                           const pa_shared_plan_info* info, const void* key_new,
+                           const void* value_new, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
 /* The kernel family pa_decode_ex(..., kernel, ...) runs for a cache `desc`,
  * num_seqs sequences of num_heads query heads and a query buffer at `query`
  * (its address only decides the 16-byte alignment the tensor-core kernel
@@ -474,10 +553,16 @@ const char* pa_status_string(pa_status status);
  * (stage), 5 scores read (stage), 6 P written (stage), 16 stage's P.V added
  * (stage), 7 item output written (item number); warps 3..5: 19 P written
  * (warp << 16 | stage), 22 item output written (warp << 16 | item number);
- * warps 2..5: 21 item entry read (warp << 16 | item number).  Entries beyond a warp's events are left as they
- * were.  A launch whose grid needs more than `bytes` records nothing.  NULL
- * turns tracing off (the default).  Host-side setting shared by all threads
- * of the process. */
+ * warps 2..5: 21 item entry read (warp << 16 | item number).  The group
+ * kernel of pa_decode_shared records its CTAs (flattened grid index) from
+ * record 2 * SMs on: producer 30 start (global timer, ns), 31 prologue done
+ * (its stages), 32 stage slot free (stage), 33 stage's boxes issued, 34 next
+ * stage's blocks resolved; MMA issuer 35 QK issued (stage), 36 PV issued
+ * (stage); softmax warps 2..5: 37 query rows stored, 38 scores ready
+ * (stage), 39 stage maximum found, 40 P written, 41 partials written.
+ * Entries beyond a warp's events are left as they were.  A launch whose grid
+ * needs more than `bytes` records nothing.  NULL turns tracing off (the
+ * default).  Host-side setting shared by all threads of the process. */
 pa_status pa_set_decode_trace(void* device_buffer, size_t bytes, int32_t events_per_role);
 
 /* Limit, in SM clock cycles, of every pipeline wait of the tensor-core decode

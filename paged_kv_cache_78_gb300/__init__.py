@@ -50,7 +50,8 @@ EXPORTS = (
     "pa_pool_is_cached", "pa_pool_free_queue", "pa_pool_reset_prefix_cache", "pa_pool_usage",
     "pa_swap_blocks", "pa_pool_set_cpu_blocks", "pa_pool_swap_out", "pa_pool_swap_in",
     "pa_pool_is_swapped", "pa_pool_num_free_cpu", "pa_decode_append", "pa_copy_bytes",
-    "pa_set_decode_wait_limit",
+    "pa_set_decode_wait_limit", "pa_decode_shared_plan", "pa_decode_shared_workspace_size",
+    "pa_decode_shared",
 )
 
 
@@ -62,6 +63,12 @@ class PAError(RuntimeError):
 
 class OutOfBlocks(PAError):
     pass
+
+
+class SharedPlanInfo(ctypes.Structure):
+    _fields_ = [("num_chunks", ctypes.c_int32), ("num_members", ctypes.c_int32),
+                ("min_shared_tokens", ctypes.c_int32), ("min_chunk_stages", ctypes.c_int32),
+                ("group_size", ctypes.c_int32), ("plan_ints", ctypes.c_int32)]
 
 
 class CacheDesc(ctypes.Structure):
@@ -104,6 +111,12 @@ def _load() -> ctypes.CDLL:
         "pa_get_device_error": [ctypes.POINTER(ctypes.c_uint32), vp],
         "pa_set_decode_trace": [vp, sz, i32],
         "pa_set_decode_wait_limit": [i64],
+        "pa_decode_shared_plan": [vp, i32, vp, i32, i32, i32, i32, i32, vp, sz,
+                                  ctypes.POINTER(SharedPlanInfo)],
+        "pa_decode_shared_workspace_size": [desc, i32, i32, i32, ctypes.POINTER(SharedPlanInfo),
+                                            p_sz],
+        "pa_decode_shared": [vp, vp, vp, desc, vp, i32, vp, i32, i32, f32, i32, vp,
+                             ctypes.POINTER(SharedPlanInfo), vp, vp, vp, sz, vp],
         "pa_pool_add_seq_tokens": [vp, vp, i64, p_i64, p_i64],
         "pa_pool_append_token_id": [vp, i64, i32, p_i64, vp],
         "pa_pool_is_cached": [vp, i32, p_i32],
@@ -356,6 +369,97 @@ def pa_decode_append(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor
                                 s, hq, float(scale), int(max_seq_len), int(partition_size),
                                 _dev_ptr(key_new, "key_new"), _dev_ptr(value_new, "value_new"),
                                 ws_ptr, ws_bytes, int(kernel), _stream(stream)), "pa_decode_append")
+
+
+SHARED_TILE_ROWS = 128
+
+
+class SharedPlan:
+    """pa_decode_shared_plan on host block tables and lengths: the plan
+    (int32, host) and its sizes; `upload` gives the device copy the decode
+    reads."""
+
+    def __init__(self, block_tables, seq_lens, block_size: int, num_heads: int,
+                 num_kv_heads: int, min_shared_blocks: int = 8):
+        bt = torch.as_tensor(block_tables).to(torch.int32).contiguous().cpu()
+        sl = torch.as_tensor(seq_lens).to(torch.int32).contiguous().cpu()
+        if bt.dim() != 2 or sl.shape != (bt.shape[0],):
+            raise ValueError("block_tables must be [num_seqs, max_blocks], seq_lens [num_seqs]")
+        n = bt.shape[0]
+        self.plan = torch.zeros(4 + 6 * n, dtype=torch.int32)
+        self.info = SharedPlanInfo()
+        _check(lib.pa_decode_shared_plan(bt.data_ptr(), bt.shape[1], sl.data_ptr(), n, block_size,
+                                         num_heads, num_kv_heads, min_shared_blocks,
+                                         self.plan.data_ptr(), self.plan.numel(),
+                                         ctypes.byref(self.info)), "pa_decode_shared_plan")
+        self.plan = self.plan[:self.info.plan_ints].clone()
+
+    @property
+    def num_chunks(self) -> int:
+        return int(self.info.num_chunks)
+
+    def chunks(self):
+        """[(first member index, members, shared tokens, group)] per chunk."""
+        nc = self.num_chunks
+        return [tuple(int(x) for x in self.plan[4 + 4 * c:8 + 4 * c]) for c in range(nc)]
+
+    def seq_start(self):
+        nc, n = self.num_chunks, int(self.plan[1])
+        return self.plan[4 + 4 * nc:4 + 4 * nc + n].tolist()
+
+    def members(self):
+        nc, n = self.num_chunks, int(self.plan[1])
+        return self.plan[4 + 4 * nc + n:].tolist()
+
+    def upload(self, device="cuda") -> torch.Tensor:
+        return self.plan.to(device)
+
+
+def pa_decode_shared_workspace_size(cache_or_desc, num_seqs: int, num_heads: int,
+                                    max_seq_len: int, plan: SharedPlan) -> int:
+    desc = cache_or_desc if isinstance(cache_or_desc, CacheDesc) else cache_desc(cache_or_desc)
+    out = ctypes.c_size_t()
+    _check(lib.pa_decode_shared_workspace_size(ctypes.byref(desc), num_seqs, num_heads,
+                                               int(max_seq_len), ctypes.byref(plan.info),
+                                               ctypes.byref(out)),
+           "pa_decode_shared_workspace_size")
+    return out.value
+
+
+def pa_decode_shared(out: torch.Tensor, query: torch.Tensor, cache: torch.Tensor,
+                     block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     max_seq_len: int, plan: SharedPlan, plan_dev: torch.Tensor,
+                     workspace: torch.Tensor | None, key_new: torch.Tensor | None = None,
+                     value_new: torch.Tensor | None = None, stream=None) -> None:
+    """pa_decode with the blocks the plan's groups share attended once per
+    group (plan_dev: the plan's device copy, SharedPlan.upload)."""
+    desc = cache_desc(cache)
+    s, hq, d = query.shape
+    if out.shape != query.shape or d != desc.head_size:
+        raise ValueError("query/out must be [num_seqs, num_heads, head_size]")
+    if query.dtype != cache.dtype or out.dtype != cache.dtype:
+        raise TypeError("query/out dtype must match the cache")
+    if block_tables.dim() != 2 or block_tables.shape[0] != s or seq_lens.shape != (s,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks], seq_lens [num_seqs]")
+    if (key_new is None) != (value_new is None):
+        raise ValueError("key_new and value_new go together")
+    kn = vn = None
+    if key_new is not None:
+        if key_new.shape != (s, desc.num_kv_heads, d) or value_new.shape != key_new.shape:
+            raise ValueError("key_new/value_new must be [num_seqs, num_kv_heads, head_size]")
+        kn, vn = _dev_ptr(key_new, "key_new"), _dev_ptr(value_new, "value_new")
+    if plan_dev.numel() < plan.info.plan_ints:
+        raise ValueError("plan_dev is shorter than the plan")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check(lib.pa_decode_shared(_dev_ptr(out, "out"), _dev_ptr(query, "query"),
+                                _dev_ptr(cache, "cache"), ctypes.byref(desc),
+                                _dev_ptr(block_tables, "block_tables", torch.int32),
+                                block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens", torch.int32),
+                                s, hq, float(scale), int(max_seq_len),
+                                _dev_ptr(plan_dev, "plan", torch.int32), ctypes.byref(plan.info),
+                                kn, vn, ws_ptr, ws_bytes, _stream(stream)), "pa_decode_shared")
 
 
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "decode_kernel.cuh"
+#include "decode_shared_kernel.cuh"
 #include "decode_tc_kernel.cuh"
 #include "pa.h"
 #include "pa_launch.h"
@@ -219,6 +220,71 @@ size_t workspace_bytes_for(int num_seqs, int num_heads, int head_size, int max_p
   const size_t rows = (size_t)num_seqs * num_heads * max_parts;
   return kWorkspaceHeader + partial_o_bytes(num_seqs, num_heads, head_size, max_parts) +
          (rows * 4 + 255) / 256 * 256 + (pairs * 4 + 255) / 256 * 256;
+}
+
+// The tensor-core kernels' map of the pool: one block's K and V rows, every
+// 128-byte column group, in one box, laid out per 8-token chunk as
+// [column group][K rows][V rows] (each 8 rows one 1024-byte swizzle atom).
+// Dimensions, innermost first: 64 elements; token within an 8-token chunk;
+// K or V; (KV head, column group); 8-token chunk of the plane
+// (block * block_size / 8 + chunk within the block).  R = rows of a box.
+CUresult encode_tc_kv_map(EncodeTiledFn encode, const pa_cache_desc* desc, const void* cache,
+                          int R, CUtensorMap* map) {
+  const int D = desc->head_size;
+  const int BS = desc->block_size;
+  const cuuint64_t row = (cuuint64_t)desc->num_kv_heads * D * 2;
+  const cuuint64_t tdim[5] = {64ull, 8ull, 2ull, (cuuint64_t)desc->num_kv_heads * (D / 64),
+                              (cuuint64_t)desc->num_blocks * (cuuint64_t)(BS / 8)};
+  const cuuint64_t tstride[4] = {row, (cuuint64_t)desc->num_blocks * BS * row, 128ull, 8 * row};
+  const cuuint32_t tbox[5] = {64u, 8u, 2u, (cuuint32_t)(D / 64), (cuuint32_t)(R / 8)};
+  const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), tdim, tstride,
+                tbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// The tensor-core decode next to a shared-prefix decode's group kernel: it
+// skips the groups' members (seq_start > 0) and decodes the other sequences
+// (the balanced split for batches of up to 256 sequences), recording their
+// partial counts next to the members' in the same array.
+struct CascadeArgs {
+  const int32_t* seq_start;
+  int32_t* counts;
+  float* part_o;
+  float* part_lse;
+  int max_parts;
+};
+
+// Stage ranges per (chunk, KV head) of the group kernel: enough CTAs to fill
+// the SMs, no more ranges than the shortest chunk has stages, at most 16 (the
+// reduce then takes rows of up to 16 partials).
+int shared_ranges(const pa_cache_desc* d, const pa_shared_plan_info* info, int num_sms) {
+  const long long units = (long long)info->num_chunks * d->num_kv_heads;
+  long long r = units > 0 ? num_sms / units : 1;
+  if (r > info->min_chunk_stages) r = info->min_chunk_stages;
+  if (r > 16) r = 16;
+  return r < 1 ? 1 : (int)r;
+}
+
+// Partials per row of a shared-prefix decode: the group kernel's ranges for
+// member rows, the balanced split's pieces for the others.
+int shared_max_parts(const pa_cache_desc* d, const pa_shared_plan_info* info, int num_seqs,
+                     int max_seq_len, int num_sms) {
+  const int r = shared_ranges(d, info, num_sms);
+  const int others = info->num_members < num_seqs && num_seqs <= pa::kTcLensCache
+                         ? balanced_max_parts(d, max_seq_len, num_sms)
+                         : 1;
+  return r > others ? r : others;
+}
+
+// Workspace of pa_decode_shared: the 256-byte header, fp32 partials and
+// log-sum-exp values of max_parts per row, then a partial count per pair.
+size_t shared_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                              int max_parts) {
+  const size_t rows = (size_t)num_seqs * num_heads * max_parts;
+  const size_t pairs = (size_t)num_seqs * num_kv_heads;
+  return 256 + (rows * head_size * 4 + 255) / 256 * 256 + (rows * 4 + 255) / 256 * 256 +
+         (pairs * 4 + 255) / 256 * 256;
 }
 
 // The kernel family for a decode call (desc already checked).
@@ -472,7 +538,8 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
                              int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
                              int32_t num_heads, float scale, int32_t max_seq_len,
                              int32_t partition_size, void* workspace, size_t workspace_bytes,
-                             int32_t kernel, const void* new_k, const void* new_v, void* stream) {
+                             int32_t kernel, const void* new_k, const void* new_v, void* stream,
+                             const CascadeArgs* cas = nullptr) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || num_heads < 1 || max_seq_len < 0 ||
@@ -501,6 +568,10 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
   if ((st = resolve_partition(desc, num_seqs, num_heads, max_seq_len, partition_size, sms,
                               &part)) != PA_OK)
     return st;
+  if (cas) {
+    if (!use_tc) return PA_ERR_UNSUPPORTED;
+    part = num_seqs <= pa::kTcLensCache ? PA_PARTITION_BALANCED : 0;
+  }
   bool balanced = part == PA_PARTITION_BALANCED;
   if (balanced && !use_tc) {
     // The CUDA-core kernel (a query the tensor-core kernel cannot load, or
@@ -512,7 +583,8 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     if (part >= max_seq_len) part = 0;
     balanced = false;
   }
-  const int max_parts = balanced  ? balanced_max_parts(desc, max_seq_len, sms)
+  const int max_parts = cas        ? cas->max_parts
+                        : balanced ? balanced_max_parts(desc, max_seq_len, sms)
                         : part > 0 ? (max_seq_len + part - 1) / part
                                    : 1;
   const size_t pairs = balanced ? (size_t)num_seqs * desc->num_kv_heads : 0;
@@ -520,7 +592,13 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
   float* part_lse = nullptr;
   int32_t* part_counts = nullptr;
   unsigned int* sched = nullptr;
-  if (part > 0 || balanced || use_tc) {
+  if (cas) {
+    // pa_decode_shared checked the workspace and laid out its parts.
+    sched = static_cast<unsigned int*>(workspace);
+    part_o = cas->part_o;
+    part_lse = cas->part_lse;
+    part_counts = cas->counts;
+  } else if (part > 0 || balanced || use_tc) {
     const size_t need =
         workspace_bytes_for(num_seqs, num_heads, D, part > 0 || balanced ? max_parts : 0, pairs);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
@@ -547,7 +625,7 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     R = BS < pa::kTcTokens ? BS : pa::kTcTokens;
     prm.num_stages = 3;
     prm.num_consumers = 1;
-    smem = pa::tc_smem_layout(D, prm.num_stages).total;
+    smem = pa::tc_smem_layout(D, prm.num_stages, cas != nullptr).total;
     prm.sched = sched;
     prm.trace = static_cast<unsigned long long*>(g_trace_buf.load());
     prm.trace_per_role = g_trace_per_role.load();
@@ -560,6 +638,12 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     // slots of a mixed-length batch are past a sequence's end; the kernel
     // then numbers only the real items (batches it caches in shared memory).
     prm.dense_items = !balanced && max_parts > 4 && num_seqs <= pa::kTcLensCache;
+    if (cas) {
+      prm.seq_start = cas->seq_start;
+      prm.part_counts = cas->counts;
+      prm.dense_items = 0;
+      if (!balanced) prm.total_items = num_seqs * desc->num_kv_heads;  // one item per pair
+    }
     if (balanced) {
       prm.balanced = 1;
       prm.total_items = balanced_ranges(desc, sms);
@@ -630,20 +714,7 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
   const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
   CUresult cr;
   if (use_tc) {
-    // The tensor-core kernel's map puts one block's K and V rows, every
-    // 128-byte column group, in one box, laid out per 8-token chunk as
-    // [column group][K rows][V rows] (each 8 rows one 1024-byte swizzle
-    // atom).  Dimensions, innermost first: 64 elements; token within an
-    // 8-token chunk; K or V; (KV head, column group); 8-token chunk of the
-    // plane (block * block_size / 8 + chunk within the block).
-    const cuuint64_t row = (cuuint64_t)desc->num_kv_heads * D * es;
-    const cuuint64_t tdim[5] = {64ull, 8ull, 2ull, (cuuint64_t)desc->num_kv_heads * (D / 64),
-                                (cuuint64_t)desc->num_blocks * (cuuint64_t)(BS / 8)};
-    const cuuint64_t tstride[4] = {row, (cuuint64_t)desc->num_blocks * BS * row, 128ull, 8 * row};
-    const cuuint32_t tbox[5] = {64u, 8u, 2u, (cuuint32_t)(D / 64), (cuuint32_t)(R / 8)};
-    cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), tdim,
-                tstride, tbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cr = encode_tc_kv_map(encode, desc, cache, R, &map);
   } else if (prm.kv_boxes) {
     // CUDA-core kernel, blocks of 8 tokens or more: one box per block holds
     // its R rows of K and V for every column group, laid out
@@ -724,7 +795,7 @@ static pa_status decode_impl(void* out, const void* query, const void* cache,
     e = pa::launch_decode_f32(D, group, grid, smem, s, map, prm, &supported);
   if (!supported) return PA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (part > 0 || (balanced && max_parts > 1)) {
+  if (!cas && (part > 0 || (balanced && max_parts > 1))) {
     e = pa::launch_lse_reduce(desc->dtype, D, out, part_o, part_lse, seq_lens, part_counts, group,
                               num_seqs, num_heads, balanced ? 0 : part, max_parts, s, &supported);
     if (!supported) return PA_ERR_UNSUPPORTED;
@@ -754,6 +825,140 @@ pa_status pa_decode_append(void* out, const void* query, void* cache, const pa_c
   return decode_impl(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                      num_heads, scale, max_seq_len, partition_size, workspace, workspace_bytes,
                      kernel, key_new, value_new, stream);
+}
+
+pa_status pa_decode_shared_workspace_size(const pa_cache_desc* desc, int32_t num_seqs,
+                                          int32_t num_heads, int32_t max_seq_len,
+                                          const pa_shared_plan_info* info, size_t* bytes) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (!bytes || !info || num_seqs < 0 || num_heads < 1 || num_heads % desc->num_kv_heads != 0 ||
+      info->num_chunks < 0 || max_seq_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (info->num_chunks == 0) {
+    *bytes = workspace_bytes_for(num_seqs, num_heads, desc->head_size, 0);
+    return PA_OK;
+  }
+  int sms = 0;
+  if ((st = device_state(nullptr, &sms)) != PA_OK) return st;
+  *bytes = shared_workspace_bytes(num_seqs, num_heads, desc->num_kv_heads, desc->head_size,
+                                  shared_max_parts(desc, info, num_seqs, max_seq_len, sms));
+  return PA_OK;
+}
+
+pa_status pa_decode_shared(void* out, const void* query, void* cache, const pa_cache_desc* desc,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                           float scale, int32_t max_seq_len, const int32_t* plan,
+                           const pa_shared_plan_info* info, const void* key_new,
+                           const void* value_new, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (!info || (key_new == nullptr) != (value_new == nullptr)) return PA_ERR_INVALID_ARG;
+  if (key_new && (!aligned(key_new, 16) || !aligned(value_new, 16))) return PA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_seqs > 65535 || num_heads < 1 || max_seq_len < 0 ||
+      max_blocks_per_seq < 1 || !std::isfinite(scale) || num_heads % desc->num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !query || !cache || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
+  int32_t family = 0;
+  if ((st = select_kernel(desc, num_seqs, num_heads, query, PA_KERNEL_TENSOR, &family)) != PA_OK)
+    return st;
+  const int nc = info->num_chunks;
+  if (nc == 0)  // nothing shared: the unsplit tensor-core decode
+    return decode_impl(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, num_heads, scale, max_seq_len, 0, workspace, workspace_bytes,
+                       PA_KERNEL_TENSOR, key_new, value_new, stream);
+  const int group = num_heads / desc->num_kv_heads;
+  if (nc < 0 || info->num_members < nc || info->num_members > num_seqs ||
+      info->group_size != group || info->min_shared_tokens < desc->block_size ||
+      info->min_chunk_stages < 1 ||
+      info->plan_ints != 4 + 4 * nc + num_seqs + info->num_members || !plan || !aligned(plan, 4))
+    return PA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int sms = 0;
+  if ((st = device_state(&err, &sms)) != PA_OK) return st;
+  const int D = desc->head_size;
+  const int ranges = shared_ranges(desc, info, sms);
+  const int max_parts = shared_max_parts(desc, info, num_seqs, max_seq_len, sms);
+  const size_t need =
+      shared_workspace_bytes(num_seqs, num_heads, desc->num_kv_heads, D, max_parts);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t rows = (size_t)num_seqs * num_heads * max_parts;
+  float* part_o = reinterpret_cast<float*>(ws + 256);
+  float* part_lse = reinterpret_cast<float*>(ws + 256 + (rows * D * 4 + 255) / 256 * 256);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + 256 + (rows * D * 4 + 255) / 256 * 256 +
+                                               (rows * 4 + 255) / 256 * 256);
+
+  EncodeTiledFn encode = nullptr;
+  if ((st = encode_fn(&encode)) != PA_OK) return st;
+  const int R = desc->block_size < pa::kTcTokens ? desc->block_size : pa::kTcTokens;
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (encode_tc_kv_map(encode, desc, cache, R, &map) != CUDA_SUCCESS) return PA_ERR_CUDA;
+  pa::SharedParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.query = query;
+  sp.block_tables = block_tables;
+  sp.seq_lens = seq_lens;
+  sp.chunks = plan + 4;
+  sp.members = plan + 4 + 4 * (size_t)nc + num_seqs;
+  sp.out = out;
+  sp.part_o = part_o;
+  sp.part_lse = part_lse;
+  sp.part_counts = counts;
+  sp.cache_w = static_cast<uint8_t*>(cache);
+  sp.new_k = key_new;
+  sp.new_v = value_new;
+  sp.err = err;
+  sp.num_chunks = nc;
+  sp.num_members = info->num_members;
+  sp.num_seqs = num_seqs;
+  sp.num_heads = num_heads;
+  sp.num_kv_heads = desc->num_kv_heads;
+  sp.group = group;
+  sp.num_blocks = desc->num_blocks;
+  sp.block_size = desc->block_size;
+  sp.log2_block_size = ilog2(desc->block_size);
+  sp.max_blocks_per_seq = max_blocks_per_seq;
+  sp.max_parts = max_parts;
+  sp.ranges = ranges;
+  sp.box_rows = R;
+  sp.log2_box_rows = ilog2(R);
+  sp.num_stages = pa::shared_stage_slots(D);
+  sp.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  const long long limit = g_wait_limit.load();
+  sp.wait_limit = limit > 0 ? limit : pa::kWaitLimitCycles;
+  sp.trace = static_cast<unsigned long long*>(g_trace_buf.load());
+  sp.trace_per_role = g_trace_per_role.load();
+  sp.trace_bytes = g_trace_bytes.load();
+  // The decode launch after it records CTAs from 0 (at most two per SM).
+  sp.trace_cta_base = 2 * sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool supported = true;
+  const dim3 grid((unsigned)ranges, (unsigned)desc->num_kv_heads, (unsigned)nc);
+  cudaError_t e =
+      pa::launch_decode_shared(D, grid, pa::shared_smem_bytes(D), s, map, sp, &supported);
+  if (!supported) return PA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  const bool others = info->num_members < num_seqs;
+  if (others) {
+    // The sequences outside every group.
+    const CascadeArgs cas{plan + 4 + 4 * (size_t)nc, counts, part_o, part_lse, max_parts};
+    st = decode_impl(out, query, cache, desc, block_tables, max_blocks_per_seq, seq_lens,
+                     num_seqs, num_heads, scale, max_seq_len, 0, workspace, workspace_bytes,
+                     PA_KERNEL_TENSOR, key_new, value_new, stream, &cas);
+    if (st != PA_OK) return st;
+  }
+  if (ranges > 1 || others) {
+    e = pa::launch_lse_reduce(desc->dtype, D, out, part_o, part_lse, seq_lens, counts, group,
+                              num_seqs, num_heads, 0, max_parts, s, &supported);
+    if (!supported) return PA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
 }
 
 }  // extern "C"

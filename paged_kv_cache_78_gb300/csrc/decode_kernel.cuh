@@ -89,6 +89,10 @@ struct DecodeParams {
   int num_consumers;     // consumer warps that take stages (1..kConsumerWarps)
   int stage_area;        // bytes before the query buffer (stages, or the merge overlay)
   long long wait_limit;  // tensor-core kernel: SM cycles a pipeline wait may take
+  // Tensor-core kernel next to a shared-prefix decode: sequences with
+  // seq_start[s] > 0 belong to a group the group kernel covers (rows and
+  // partial counts) and are skipped; the others are decoded as usual.
+  const int32_t* seq_start;
 };
 
 // Dynamic shared memory a decode launch needs (the kernel aligns its base to 1024).

@@ -16,7 +16,8 @@ static cudaError_t launch_tc(int num_sms, int smem_bytes, cudaStream_t stream,
                              const CUtensorMap& kv_map, const CUtensorMap& q_map,
                              const DecodeParams& params) {
   static std::atomic<int> configured[64];
-  static std::atomic<int> per_sm[64];
+  static std::atomic<int> smem_per_sm[64];
+  static std::atomic<int> ctas_by_regs[64];
   auto kernel = paged_decode_tc_kernel<D, GP, kBal, kTrace>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -28,25 +29,28 @@ static cudaError_t launch_tc(int num_sms, int smem_bytes, cudaStream_t stream,
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    configured[dev].store(smem_bytes, std::memory_order_relaxed);
-    // Resident CTAs per SM: bounded by shared memory (plus the 1 KB the
-    // driver reserves per CTA), registers and tensor-memory columns.
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return e;
-    int smem_per_sm = 0, regs_per_sm = 0;
-    e = cudaDeviceGetAttribute(&smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    int sm_smem = 0, regs_per_sm = 0;
+    e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
     if (e != cudaSuccess) return e;
     const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;
-    int blocks = smem_per_sm / (smem_bytes + 1024);
-    blocks = std::min(blocks, regs_per_sm / (regs_per_warp * (kTcThreads / 32)));
-    blocks = std::min(blocks, 512 / kTcTmemCols);
-    per_sm[dev].store(blocks < 1 ? 1 : blocks, std::memory_order_relaxed);
+    smem_per_sm[dev].store(sm_smem, std::memory_order_relaxed);
+    ctas_by_regs[dev].store(regs_per_sm / (regs_per_warp * (kTcThreads / 32)),
+                            std::memory_order_relaxed);
+    configured[dev].store(smem_bytes, std::memory_order_relaxed);
   }
+  // Resident CTAs per SM at this launch's shared memory (plus the 1 KB the
+  // driver reserves per CTA), registers and tensor-memory columns.
+  int per_sm = smem_per_sm[dev].load(std::memory_order_relaxed) / (smem_bytes + 1024);
+  per_sm = std::min(per_sm, ctas_by_regs[dev].load(std::memory_order_relaxed));
+  per_sm = std::min(per_sm, 512 / kTcTmemCols);
+  if (per_sm < 1) per_sm = 1;
   // Persistent grid: as many CTAs as fit at once, at most one per work item.
-  long long grid = (long long)num_sms * per_sm[dev].load(std::memory_order_relaxed);
+  long long grid = (long long)num_sms * per_sm;
   if (grid > params.total_items) grid = params.total_items;
   if (grid < 1) return cudaSuccess;
   DecodeParams prm = params;

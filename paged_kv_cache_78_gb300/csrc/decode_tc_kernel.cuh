@@ -72,10 +72,15 @@ struct TcSmem {
   int misc_off;
   int lens_off;  // cached sequence lengths (batches of up to kTcLensCache)
   int pre_off;   // work items before each sequence (dense numbering), kTcLensCache + 1
+  int starts_off;  // cached first tokens of each sequence's own part (after a shared prefix)
   int total;     // bytes to request (includes 1024 of alignment slack)
 };
 
-__host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages) {
+// with_starts: room for the own-part start tokens of a launch after a
+// shared-prefix decode (other launches leave it out: at head size 64 the
+// extra kilobyte would cost the second resident CTA of an SM).
+__host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages,
+                                                 bool with_starts = false) {
   TcSmem l;
   const int groups = head_size / 64;
   l.region = groups * kTcTokens * 128;
@@ -90,7 +95,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages) 
   l.misc_off = l.bar_off + 8 * (2 * num_stages + 14 + 2 * kTcItemRing + 1);
   l.lens_off = l.misc_off + 64;
   l.pre_off = l.lens_off + kTcLensCache * 4;
-  l.total = l.pre_off + (kTcLensCache + 4) * 4 + 1024;
+  l.starts_off = l.pre_off + (kTcLensCache + 4) * 4;
+  l.total = l.starts_off + (with_starts ? kTcLensCache * 4 : 0) + 1024;
   return l;
 }
 
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int lane = tid & 31;
   const int G = p.group;
   const int NS = p.num_stages;
-  const TcSmem lay = tc_smem_layout(D, NS);
+  const TcSmem lay = tc_smem_layout(D, NS, p.seq_start != nullptr);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -330,8 +336,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Sequence lengths in shared memory, so classifying a work item needs no
   // global load.
   int* lens_s = p.num_seqs <= kTcLensCache ? reinterpret_cast<int*>(base + lay.lens_off) : nullptr;
+  // After a shared-prefix decode, the first token of each sequence's own part.
+  int* starts_s =
+      (p.seq_start != nullptr && lens_s) ? reinterpret_cast<int*>(base + lay.starts_off) : nullptr;
   if (lens_s)
-    for (int i = tid; i < p.num_seqs; i += kTcThreads) lens_s[i] = p.seq_lens[i];
+    for (int i = tid; i < p.num_seqs; i += kTcThreads) {
+      lens_s[i] = p.seq_lens[i];
+      if (starts_s) starts_s[i] = p.seq_start[i];
+    }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
@@ -390,7 +402,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ((L + BS - 1) >> l2bs) > p.max_blocks_per_seq)) {
             if (blockIdx.x == 0) record_error(p.err, PA_DEVERR_SEQ_LEN);
           } else if (bal) {
-            n = L <= 0 ? 0 : ((L + kTcTokens - 1) / kTcTokens) * p.num_kv_heads;
+            // Members of a shared-prefix group (start > 0) are the group
+            // kernel's: no stages here.
+            const bool member = starts_s && starts_s[sq] > 0;
+            n = (L <= 0 || member) ? 0 : ((L + kTcTokens - 1) / kTcTokens) * p.num_kv_heads;
           } else {
             n = np * p.num_kv_heads;
           }
@@ -473,7 +488,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         } else if (zs < p.num_seqs) {
-          if (pre[zs + 1] == pre[zs] || overflow) {
+          if (starts_s && starts_s[zs] > 0 && lens_s[zs] > 0 && !overflow) {
+            // A shared-prefix group member: the group kernel's rows and counts.
+            skip = true;
+            zs += (int)gridDim.x;
+          } else if (pre[zs + 1] == pre[zs] || overflow) {
             // No stages: zero rows for length 0 (a length error leaves its
             // rows undefined); no partials either way.
             if (lane == 0) p.part_counts[zs * p.num_kv_heads + zh] = 0;
@@ -536,6 +555,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           it.nstages = (it.tok1 - it.tok0 + kTcTokens - 1) / kTcTokens;
           it.final_out = nparts == 1;
           wnew = p.new_k != nullptr && it.tok1 == L;
+        }
+        if (p.seq_start != nullptr && it.part == 0) {
+          // Next to a shared-prefix decode: members of a group (start > 0)
+          // are the group kernel's; the others' rows are final here.
+          const int st = starts_s ? starts_s[it.s] : __ldg(p.seq_start + it.s);
+          if (st > 0 && L > 0) skip = true;
+          else p.part_counts[it.s * p.num_kv_heads + it.h] = 0;
         }
       }
       if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 10, bal ? (uint32_t)bg : idx);
@@ -647,13 +673,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int st_n = min(kTcTokens, it.tok1 - st_tok);
         const int nbox = (st_n + R - 1) >> log2R;
         const int lb0 = st_tok >> l2bs;
-        if (wnew && k == it.nstages - 1)  // the newest token lands in this stage: write it first
-          write_new_token(p.cache_w, p.new_k, p.new_v, table, it.s, it.h, it.tok1 - 1,
-                          p.num_kv_heads, D * 2 / 16, BS, l2bs, p.num_blocks, p.err, lane);
         while (lb0 >= win + 32) {
           cur = nxt;
           win += 32;
           nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
+        }
+        if (wnew && k == it.nstages - 1) {
+          // The newest token lands in this stage: write it first, into the
+          // block the table window already holds (at most 48 blocks past win).
+          const int src = ((it.tok1 - 1) >> l2bs) - win;
+          const int id_cur = __shfl_sync(0xffffffffu, cur, src & 31);
+          const int id_nxt = __shfl_sync(0xffffffffu, nxt, src & 31);
+          write_new_token_in(p.cache_w, p.new_k, p.new_v, src < 32 ? id_cur : id_nxt, it.s, it.h,
+                             it.tok1 - 1, p.num_kv_heads, D * 2 / 16, BS, p.num_blocks, p.err,
+                             lane);
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)nbox * box_bytes);

@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Prefetch a 5-D box of the map into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                   int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 // ---- loads ------------------------------------------------------------------
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -176,6 +186,30 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // `chunks` chunks), then make the writes visible to TMA reads by the warp.
 // The slot's block comes from the sequence's table row; an id outside the
 // pool skips the write and records PA_DEVERR_BLOCK_ID.  Whole warp.
+// write_new_token with the slot's block id already known (id, warp-uniform).
+__device__ __forceinline__ void write_new_token_in(uint8_t* cache, const void* new_k,
+                                                   const void* new_v, int id, int s, int h,
+                                                   int pos, int num_kv_heads, int chunks,
+                                                   int block_size, int num_blocks,
+                                                   unsigned int* err, int lane) {
+  const bool ok = id >= 0 && id < num_blocks;
+  if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+  const size_t row_bytes = (size_t)num_kv_heads * chunks * 16;
+  for (int i = lane; ok && i < 2 * chunks; i += 32) {
+    const int kv = i >= chunks;
+    const int c = i - kv * chunks;
+    const uint4* src = reinterpret_cast<const uint4*>(kv ? new_v : new_k) +
+                       ((size_t)s * num_kv_heads + h) * chunks + c;
+    uint8_t* dst = cache + (size_t)kv * num_blocks * block_size * row_bytes +
+                   ((size_t)id * block_size + (pos & (block_size - 1))) * row_bytes +
+                   (size_t)h * chunks * 16 + (size_t)c * 16;
+    stg_v4(dst, ldg_nc_v4(src));
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+  fence_proxy_async_global();
+}
+
 __device__ __forceinline__ void write_new_token(uint8_t* cache, const void* new_k,
                                                 const void* new_v, const int32_t* table_row,
                                                 int s, int h, int pos, int num_kv_heads,

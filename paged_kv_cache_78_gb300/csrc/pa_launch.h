@@ -56,6 +56,16 @@ cudaError_t launch_decode_tc(int head_size, int num_sms, int smem_bytes, cudaStr
                              const CUtensorMap& kv_map, const CUtensorMap& q_map,
                              const DecodeParams& params, bool* supported);
 
+// Shared-prefix decode (bf16, head size 64 or 128): grid = (stage ranges,
+// KV heads, chunks).  shared_stage_slots / shared_smem_bytes give its stage
+// ring and dynamic shared memory.
+struct SharedParams;
+int shared_stage_slots(int head_size);
+int shared_smem_bytes(int head_size);
+cudaError_t launch_decode_shared(int head_size, dim3 grid, int smem_bytes, cudaStream_t stream,
+                                 const CUtensorMap& kv_map, const SharedParams& params,
+                                 bool* supported);
+
 // Log-sum-exp reduce of split-KV partials.  A row's partial count comes from
 // counts[row / group] when counts is given (balanced split), else from its
 // sequence length and partition_tokens.

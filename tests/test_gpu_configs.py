@@ -155,20 +155,32 @@ def replay_script(script, num_heads, num_kv_heads, head_size, seed):
     assert pa.pa_get_device_error() == 0
     want = oracle.decode(q, cache_ref, bt.numpy(), sl.numpy(), scale)
     assert_close(to_f64(out), want, "bf16", "shared prefix decode")
-    return copies
+    # The same batch through the shared-prefix decode: the blocks the pool
+    # shares are attended once per group of sharers.
+    plan = pa.SharedPlan(bt, sl, bs, num_heads, num_kv_heads)
+    ws2 = pa.alloc_workspace(pa.pa_decode_shared_workspace_size(cache_dev, len(seqs), num_heads,
+                                                                max_len, plan), "cuda")
+    out2 = torch.empty_like(out)
+    pa.pa_decode_shared(out2, to_device(q), cache_dev, bt.cuda(), sl.cuda(), scale, max_len, plan,
+                        plan.upload(), ws2)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert_close(to_f64(out2), want, "bf16", "shared-prefix decode (shared blocks once per group)")
+    return copies, plan.num_chunks
 
 
 def test_parallel_sampling_with_copy_on_write():
     script = workloads.shared_prefix_script(variant="fork", prompt_len=1018)
-    copies = replay_script(script, 32, 8, 128, seed=30)
+    copies, chunks = replay_script(script, 32, 8, 128, seed=30)
     assert copies == 16 * 7  # the partly filled last prompt block: one copy per extra sample
+    assert chunks == 16
 
 
 def test_parallel_sampling_full_prompt_blocks_need_no_copy():
     script = workloads.shared_prefix_script(variant="fork", prompt_len=1024, num_requests=4)
-    assert replay_script(script, 32, 8, 128, seed=31) == 0
+    assert replay_script(script, 32, 8, 128, seed=31) == (0, 4)
 
 
 def test_shared_prefix_requests():
     script = workloads.shared_prefix_script(variant="prefix")
-    assert replay_script(script, 32, 8, 128, seed=32) == 0
+    assert replay_script(script, 32, 8, 128, seed=32) == (0, 4)
