@@ -550,8 +550,10 @@ const char* pa_status_string(pa_status status);
  * (stage), 8 producer done (items).  MMA issuer: 13 item taken (item
  * number), 3 QK issued (stage), 17 P.V inputs ready (stage), 4 PV issued
  * (stage).  Softmax warp 2: 14 item taken (item number), 15 scores ready
- * (stage), 5 scores read (stage), 6 P written (stage), 16 stage's P.V added
- * (stage), 7 item output written (item number); warps 3..5: 19 P written
+ * (stage), 5 scores read (stage), 24 maximum check done (stage), 25 P
+ * stored to shared memory (stage), 6 P published (stage), 16 item's O read
+ * from tensor memory (last stage), 7 item output written (item number);
+ * warps 3..5: 19 P written
  * (warp << 16 | stage), 22 item output written (warp << 16 | item number);
  * warps 2..5: 21 item entry read (warp << 16 | item number).  The group
  * kernel of pa_decode_shared records its CTAs (flattened grid index) from
@@ -559,7 +561,10 @@ const char* pa_status_string(pa_status status);
  * (its stages), 32 stage slot free (stage), 33 stage's boxes issued, 34 next
  * stage's blocks resolved; MMA issuer 35 QK issued (stage), 36 PV issued
  * (stage); softmax warps 2..5: 37 query rows stored, 38 scores ready
- * (stage), 39 stage maximum found, 40 P written, 41 partials written.
+ * (stage), 43 stage's masks built (stage), 39 stage's weights written to
+ * tensor memory (stage), 46 O rescale stores issued (stage), 47 O rescale
+ * stores done (stage), 40 P published (stage), 42 last P.V done, 41 rows or
+ * partials written.
  * Entries beyond a warp's events are left as they were.  A launch whose grid
  * needs more than `bytes` records nothing.  NULL turns tracing off (the
  * default).  Host-side setting shared by all threads of the process. */

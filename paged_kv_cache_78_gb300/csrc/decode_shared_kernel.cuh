@@ -485,7 +485,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
         meta[slot * kShMaxBoxes + lane] = x.live ? ((x.owner + 1) << 16) | x.cnt : 0;
       const unsigned live_mask = __ballot_sync(0xffffffffu, x.live);
       // The fused cache write of each member whose newest token is here, into
-      // the block the box is loaded from.
+      // the block the box is loaded from (its rows were fetched into L2 a
+      // stage earlier, so each load is an L2 hit).
       unsigned wmask = __ballot_sync(0xffffffffu, x.live && x.last && p.new_k != nullptr);
       while (wmask) {
         const int b = __ffs(wmask) - 1;
@@ -493,8 +494,12 @@ __global__ void __launch_bounds__(kShThreads, 1)
         const int ws = __shfl_sync(0xffffffffu, x.seq, b);
         const int wpos = __shfl_sync(0xffffffffu, x.tok + x.cnt - 1, b);
         const int wid = __shfl_sync(0xffffffffu, x.id, b);
-        write_new_token_in(p.cache_w, p.new_k, p.new_v, wid, ws, h, wpos, p.num_kv_heads,
-                           D * 2 / 16, BS, p.num_blocks, p.err, lane);
+        const uint4 wv = load_new_token(p.new_k, p.new_v, ws, h, p.num_kv_heads, D * 2 / 16, lane);
+        store_new_token(p.cache_w, wv, wid, h, wpos, p.num_kv_heads, D * 2 / 16, BS, p.num_blocks,
+                        p.err, lane);
+        fence_proxy_async_global();
+        __syncwarp();
+        fence_proxy_async_global();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(full0 + 8u * slot, (uint32_t)__popc(live_mask) * box_bytes);
@@ -521,6 +526,15 @@ __global__ void __launch_bounds__(kShThreads, 1)
         if (nx.live && nx.id >= 0 && nx.id < p.num_blocks)
           tma_prefetch_l2_5d(&kv_map, 0, 0, 0, h * kGroups,
                              nx.id * chunks_per_block + ((nx.tok & (BS - 1)) >> 3));
+        if (nx.live && nx.last && p.new_k != nullptr) {
+          // The rows that stage writes (D * 2 bytes each of K and V).
+          const size_t row = ((size_t)nx.seq * p.num_kv_heads + h) * (D * 2);
+#pragma unroll
+          for (int c = 0; c < D * 2; c += 128) {
+            prefetch_l2(static_cast<const uint8_t*>(p.new_k) + row + c);
+            prefetch_l2(static_cast<const uint8_t*>(p.new_v) + row + c);
+          }
+        }
       }
       if (lane == 0) sh_trace<kTrace>(p, 0, ntr, 34, (uint32_t)k);
     }

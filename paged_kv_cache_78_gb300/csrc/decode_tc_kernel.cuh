@@ -90,9 +90,9 @@ __host__ __device__ inline TcSmem tc_smem_layout(int head_size, int num_stages,
   l.red_off = l.p_off + 2 * 2 * kTcHeads * 128;
   l.item_off = l.red_off + 3 * 4 * kTcHeads * 4;
   l.bar_off = l.item_off + kTcItemRing * (int)sizeof(TcItem);
-  // full[NS], empty[NS], s/p/o full/free and q full/free [2 each], item
-  // full/free [ring], drain
-  l.misc_off = l.bar_off + 8 * (2 * num_stages + 14 + 2 * kTcItemRing + 1);
+  // full[NS], empty[NS], s full/free, p full, o full and q full/free [2
+  // each], item full/free [ring], drain
+  l.misc_off = l.bar_off + 8 * (2 * num_stages + 12 + 2 * kTcItemRing + 1);
   l.lens_off = l.misc_off + 64;
   l.pre_off = l.lens_off + kTcLensCache * 4;
   l.starts_off = l.pre_off + (kTcLensCache + 4) * 4;
@@ -165,8 +165,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 // Barrier addresses of the tensor-core decode (shared-memory byte addresses).
 struct TcBars {
-  uint32_t full0, empty0, s_full, s_free, p_full, o_full, o_free, q_full, q_free, it_full,
-      it_free, drain;
+  uint32_t full0, empty0, s_full, s_free, p_full, o_full, q_full, q_free, it_full, it_free,
+      drain;
   __device__ __forceinline__ TcBars(uint32_t base, int ns) {
     full0 = base;
     empty0 = base + 8u * ns;
@@ -174,10 +174,9 @@ struct TcBars {
     s_free = s_full + 16;
     p_full = s_full + 32;
     o_full = s_full + 48;
-    o_free = s_full + 64;
-    q_full = s_full + 80;
-    q_free = s_full + 96;
-    it_full = s_full + 112;
+    q_full = s_full + 64;
+    q_free = s_full + 80;
+    it_full = s_full + 96;
     it_free = it_full + 8u * kTcItemRing;
     drain = it_free + 8u * kTcItemRing;
   }
@@ -213,26 +212,6 @@ __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
-}
-
-// Softmax warpgroup: add the PV tile of global stage gk (tensor-memory buffer
-// gk % 2) into the fp32 accumulator, rescaled by that stage's factor.
-template <int GP>
-__device__ __forceinline__ bool tc_epilogue(int gk, const TcBars& b, uint32_t t_o_lane,
-                                            unsigned int* err, long long limit,
-                                            float (&o_acc)[GP], const float (&alpha)[GP]) {
-  const int sb = gk & 1;
-  const bool w = mbar_wait_bounded(b.o_full + 8u * sb, (gk >> 1) & 1, err, limit);
-  __syncwarp();
-  tc::fence_after_sync();
-  float ot[GP];
-  tc::tmem_ld<GP>(t_o_lane + 16u * sb, ot);
-  tc::tmem_wait_ld();
-  tc::fence_before_sync();
-  mbar_arrive(b.o_free + 8u * sb);
-#pragma unroll
-  for (int g = 0; g < GP; ++g) o_acc[g] = fmaf(o_acc[g], alpha[g], ot[g]);
-  return w;
 }
 
 // GP: the query group size G rounded up to a power of two (1..16); the
@@ -289,7 +268,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bars.s_free + 8u * i, 128);
       mbar_init(bars.p_full + 8u * i, 128);
       mbar_init(bars.o_full + 8u * i, 1);
-      mbar_init(bars.o_free + 8u * i, 128);
       mbar_init(bars.q_full + 8u * i, 1);
       mbar_init(bars.q_free + 8u * i, 1);
     }
@@ -630,6 +608,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
       if (it.kind != kItemAttend) continue;
+      // The fused write's rows and target block, loaded now so that their
+      // latency overlaps the query load and the first stage's issue; stored
+      // before the item's second stage (or its only one) is issued, fenced
+      // before its last.
+      uint4 new_kv = make_uint4(0u, 0u, 0u, 0u);
+      int new_id = 0, k_store = -1, k_fence = -1;
+      if (wnew) {
+        new_kv = load_new_token(p.new_k, p.new_v, it.s, it.h, p.num_kv_heads, D * 2 / 16, lane);
+        new_id = __ldg(table + lb_end - 1);
+        k_store = min(1, it.nstages - 1);
+        k_fence = it.nstages - 1;
+      }
 
       // Query rows h*G .. h*G+15 of sequence s (rows past G are masked).
       const int qb = qi & 1;
@@ -678,15 +668,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           win += 32;
           nxt = (win + 32 + lane < lb_end) ? __ldg(table + win + 32 + lane) : 0;
         }
-        if (wnew && k == it.nstages - 1) {
-          // The newest token lands in this stage: write it first, into the
-          // block the table window already holds (at most 48 blocks past win).
-          const int src = ((it.tok1 - 1) >> l2bs) - win;
-          const int id_cur = __shfl_sync(0xffffffffu, cur, src & 31);
-          const int id_nxt = __shfl_sync(0xffffffffu, nxt, src & 31);
-          write_new_token_in(p.cache_w, p.new_k, p.new_v, src < 32 ? id_cur : id_nxt, it.s, it.h,
-                             it.tok1 - 1, p.num_kv_heads, D * 2 / 16, BS, p.num_blocks, p.err,
-                             lane);
+        if (k == k_store)
+          store_new_token(p.cache_w, new_kv, new_id, it.h, it.tok1 - 1, p.num_kv_heads, D * 2 / 16,
+                          BS, p.num_blocks, p.err, lane);
+        if (k == k_fence) {
+          // The newest token lands in this stage: its store is ordered before
+          // the stage's TMA reads.
+          fence_proxy_async_global();
+          __syncwarp();
+          fence_proxy_async_global();
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)nbox * box_bytes);
@@ -736,6 +726,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool leader = elect_one();
     int next_qk = 0, next_pv = 0;  // global stage counters
     int ii = 0, qi = 0, qb = 0, qk_k = 0, qk_n = 0;
+    // Bit gk % 4: stage gk is its item's first (its P.V starts the item's O
+    // accumulator instead of adding to it).  QK runs at most two ahead of PV.
+    uint32_t first_bits = 0;
     bool have_item = false, need_q = false, end_seen = false, ok = true;
     int ntr = 0;
     long long t_idle = clock64();
@@ -772,8 +765,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int gk = next_pv;
         const int slot = gk % NS;
         const int sb = gk & 1;
-        if (warp_test(bars.p_full + 8u * sb, (gk >> 1) & 1) &&
-            (gk < 2 || warp_test(bars.o_free + 8u * sb, ((gk >> 1) - 1) & 1))) {
+        if (warp_test(bars.p_full + 8u * sb, (gk >> 1) & 1)) {
           tc::fence_after_sync();
           // A: the stage's V rows read MN-major (V^T), 64-dimension groups
           // kPvLbo apart, 8-token groups kChunkBytes apart; B: P^T.
@@ -787,7 +779,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kk = 0; kk < kPvSteps; ++kk) {
               const uint32_t aoff = (uint32_t)(kk * 2 * kChunkBytes);
               const uint32_t boff = (uint32_t)((kk >> 2) * kTcHeads * 128 + (kk & 3) * 32);
-              tc::mma_bf16(tO0 + 16u * sb, a0 + (aoff >> 4), b0 + (boff >> 4), kIdescPV, kk > 0);
+              tc::mma_bf16(tO0, a0 + (aoff >> 4), b0 + (boff >> 4), kIdescPV,
+                           kk > 0 || !((first_bits >> (gk & 3)) & 1u));
             }
             tc::mma_commit(bars.o_full + 8u * sb);
             tc::mma_commit(bars.empty0 + 8u * slot);
@@ -811,6 +804,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                   16, kChunkBytes);
           const uint64_t b0 = tc::smem_desc_sw128(q_s + (uint32_t)(qb * kQTile), 16, 1024);
           const bool last = qk_k + 1 == qk_n;
+          first_bits = (first_bits & ~(1u << (gk & 3))) | ((uint32_t)(qk_k == 0) << (gk & 3));
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < kKSteps; ++kk) {
@@ -906,13 +900,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         continue;
       }
 
-      float m_run[GP], l_run[GP], o_acc[GP], alpha_prev[GP];
+      float m_run[GP], l_run[GP], o_acc[GP];
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
         m_run[g] = -INFINITY;
         l_run[g] = 0.f;
-        o_acc[g] = 0.f;
-        alpha_prev[g] = 1.f;
       }
       const int n = it.nstages;
       for (int k = 0; k < n; ++k) {
@@ -973,11 +965,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float alpha[GP], pr[GP];
 #pragma unroll
         for (int g = 0; g < GP; ++g) alpha[g] = 1.f;
-        if (softmax_group_any(need)) {
+        const bool need_any = softmax_group_any(need);
+        if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 24, (uint32_t)g_k);
+        if (need_any) {
           float* redk = red + sb * 4 * kTcHeads;
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
-            const float wm = warp_max(x[g]);
+            const float wm = warp_max_redux(x[g]);
             if (lane == 0) redk[q4 * kTcHeads + g] = wm;
           }
           if (!(ok = softmax_group_all(ws && ok && !flags[0]))) break;
@@ -991,12 +985,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (g < G) alpha[g] = fast_exp2(m_run[g] - m_new);
             m_run[g] = m_new;
           }
+          if (k >= 1) {
+            // O (in tensor memory, the sum of this item's P.V tiles so far)
+            // is rescaled to the new maximum once the previous stage's P.V
+            // has landed, before this stage's P releases the next P.V.
+            const int gp = g_k - 1;
+            const bool wo = mbar_wait_bounded(bars.o_full + 8u * (gp & 1), (gp >> 1) & 1, p.err,
+                                              p.wait_limit);
+            __syncwarp();
+            tc::fence_after_sync();
+            float ot[GP];
+            tc::tmem_ld<GP>(tO_lane, ot);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < GP; ++g) ot[g] *= alpha[g];
+            tc::tmem_st<GP>(tO_lane, ot);
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            ok = wo && ok;
+          }
+        }
+        // The weight enters P.V rounded to bf16; the denominator sums the
+        // same rounded weights, so the output stays a convex combination.
+        // Two heads' weights are rounded and packed by one conversion.
+        uint32_t pw[(GP + 1) / 2];
+#pragma unroll
+        for (int i = 0; i < (GP + 1) / 2; ++i) {
+          const int g0 = 2 * i, g1 = 2 * i + 1 < GP ? 2 * i + 1 : 2 * i;
+          const float e0 = g0 < G ? fast_exp2(x[g0] - m_run[g0]) : 0.f;
+          const float e1 = (2 * i + 1 < GP && g1 < G) ? fast_exp2(x[g1] - m_run[g1]) : 0.f;
+          pw[i] = pack_bf16x2(e0, e1);
         }
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          // The weight enters P.V rounded to bf16; the denominator sums the
-          // same rounded weights, so the output stays a convex combination.
-          pr[g] = g < G ? __bfloat162float(__float2bfloat16_rn(fast_exp2(x[g] - m_run[g]))) : 0.f;
+          pr[g] = (g & 1) ? bf16_hi(pw[g >> 1]) : bf16_lo(pw[g >> 1]);
           l_run[g] = fmaf(l_run[g], alpha[g], pr[g]);
         }
         // P^T as the PV's B operand: [64-token group][16 rows][128 bytes], swizzled.
@@ -1008,20 +1030,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int g = 0; g < GP; ++g) {
             const uint32_t addr = pb + (uint32_t)((g >> 3) * 1024 + (g & 7) * 128 +
                                                   ((((col >> 3) ^ (g & 7))) << 4) + (col & 7) * 2);
-            st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr[g])));
+            st_shared_u16(addr, (uint16_t)((g & 1) ? (pw[g >> 1] >> 16) : (pw[g >> 1] & 0xffffu)));
           }
         }
+        if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 25, (uint32_t)g_k);
         tc::fence_proxy_async_smem();
         mbar_arrive(bars.p_full + 8u * sb);
         if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 6, (uint32_t)g_k);
         else if (lane == 0) tc_trace<kTrace>(p, warp, ntr, 19, (uint32_t)((warp << 16) | g_k));
-        if (k >= 1) {
-          ok = tc_epilogue<GP>(g_k - 1, bars, tO_lane, p.err, p.wait_limit, o_acc, alpha_prev) &&
-               ok;
-          if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(g_k - 1));
-        }
-#pragma unroll
-        for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
       }
       // A failed wait above is per thread: the barrier below settles it for
       // the warpgroup (a thread leaving alone would strand the others).
@@ -1036,7 +1052,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) red2[q4 * kTcHeads + g] = s_;
       }
       if (!(ok = softmax_group_all(ok && !flags[0]))) break;
-      ok = tc_epilogue<GP>(gk + n - 1, bars, tO_lane, p.err, p.wait_limit, o_acc, alpha_prev);
+      {
+        const int gl = gk + n - 1;
+        ok = mbar_wait_bounded(bars.o_full + 8u * (gl & 1), (gl >> 1) & 1, p.err, p.wait_limit);
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_ld<GP>(tO_lane, o_acc);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+      }
       if (tid == 64) tc_trace<kTrace>(p, 2, ntr, 16, (uint32_t)(gk + n - 1));
       gk += n;
       {

@@ -116,6 +116,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // ---- TMA ------------------------------------------------------------------
 
+// Fetch the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -181,35 +186,47 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The fused write split in two, so that the load's latency can overlap other
+// work: load_new_token fetches the newest token's K and V rows of KV head h of
+// sequence s into the warp's lanes (lane i < 2 * chunks holds 16-byte chunk i,
+// keys first; 2 * chunks <= 32, i.e. rows of at most 256 bytes), and
+// store_new_token writes them into slot `pos` of block `id` (warp-uniform).
+// An id outside the pool skips the store and records PA_DEVERR_BLOCK_ID.  The
+// caller fences (fence_proxy_async_global, every lane) before a TMA read of
+// the slot.
+__device__ __forceinline__ uint4 load_new_token(const void* new_k, const void* new_v, int s,
+                                                int h, int num_kv_heads, int chunks, int lane) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < 2 * chunks) {
+    const int kv = lane >= chunks;
+    const int c = lane - kv * chunks;
+    v = ldg_nc_v4(reinterpret_cast<const uint4*>(kv ? new_v : new_k) +
+                  ((size_t)s * num_kv_heads + h) * chunks + c);
+  }
+  return v;
+}
+
+__device__ __forceinline__ void store_new_token(uint8_t* cache, uint4 v, int id, int h, int pos,
+                                                int num_kv_heads, int chunks, int block_size,
+                                                int num_blocks, unsigned int* err, int lane) {
+  const bool ok = id >= 0 && id < num_blocks;
+  if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+  if (ok && lane < 2 * chunks) {
+    const int kv = lane >= chunks;
+    const int c = lane - kv * chunks;
+    const size_t row_bytes = (size_t)num_kv_heads * chunks * 16;
+    uint8_t* dst = cache + (size_t)kv * num_blocks * block_size * row_bytes +
+                   ((size_t)id * block_size + (pos & (block_size - 1))) * row_bytes +
+                   (size_t)h * chunks * 16 + (size_t)c * 16;
+    stg_v4(dst, v);
+  }
+}
+
 // Write the newest token (position `pos` of sequence s) of KV head h into
 // its cache slot, keys and values, one 16-byte chunk per lane (rows of
 // `chunks` chunks), then make the writes visible to TMA reads by the warp.
 // The slot's block comes from the sequence's table row; an id outside the
 // pool skips the write and records PA_DEVERR_BLOCK_ID.  Whole warp.
-// write_new_token with the slot's block id already known (id, warp-uniform).
-__device__ __forceinline__ void write_new_token_in(uint8_t* cache, const void* new_k,
-                                                   const void* new_v, int id, int s, int h,
-                                                   int pos, int num_kv_heads, int chunks,
-                                                   int block_size, int num_blocks,
-                                                   unsigned int* err, int lane) {
-  const bool ok = id >= 0 && id < num_blocks;
-  if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
-  const size_t row_bytes = (size_t)num_kv_heads * chunks * 16;
-  for (int i = lane; ok && i < 2 * chunks; i += 32) {
-    const int kv = i >= chunks;
-    const int c = i - kv * chunks;
-    const uint4* src = reinterpret_cast<const uint4*>(kv ? new_v : new_k) +
-                       ((size_t)s * num_kv_heads + h) * chunks + c;
-    uint8_t* dst = cache + (size_t)kv * num_blocks * block_size * row_bytes +
-                   ((size_t)id * block_size + (pos & (block_size - 1))) * row_bytes +
-                   (size_t)h * chunks * 16 + (size_t)c * 16;
-    stg_v4(dst, ldg_nc_v4(src));
-  }
-  fence_proxy_async_global();
-  __syncwarp();
-  fence_proxy_async_global();
-}
-
 __device__ __forceinline__ void write_new_token(uint8_t* cache, const void* new_k,
                                                 const void* new_v, const int32_t* table_row,
                                                 int s, int h, int pos, int num_kv_heads,
@@ -241,6 +258,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Maximum of v over the full warp, in one warp reduction instruction.
+__device__ __forceinline__ float warp_max_redux(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// lo and hi rounded to bf16 (nearest even) and packed, lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // The two bf16 halves of a 32-bit word as fp32 (exact).
