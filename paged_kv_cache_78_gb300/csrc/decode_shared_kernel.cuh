@@ -146,16 +146,12 @@ __device__ __forceinline__ float sh_tree_max(const float* v) {
   }
 }
 
-// A full stage (every column kept): the row's 128 scores read at once, their
-// maximum, then the weights of all of them from the same registers.  Whole
-// warp.
-__device__ __forceinline__ float sh_full_stage(uint32_t srow, float scale_log2, float& m_run,
-                                               float& l_run, float& alpha, bool& rescale,
-                                               int k, uint32_t prow) {
-  float x[kShTokens];
-#pragma unroll
-  for (int c = 0; c < kShTokens / 32; ++c) tc::tmem_ld<32>(srow + (uint32_t)(c * 32), x + 32 * c);
-  tc::tmem_wait_ld();
+// A full stage (every column kept): the row's 128 scores (read at once by
+// the caller), their maximum, then the weights of all of them from the same
+// registers.  Whole warp.
+__device__ __forceinline__ float sh_full_stage(float (&x)[kShTokens], float scale_log2,
+                                               float& m_run, float& l_run, float& alpha,
+                                               bool& rescale, int k, uint32_t prow) {
 #pragma unroll
   for (int c = 0; c < kShTokens; ++c) x[c] *= scale_log2;
   const float mx = sh_tree_max<kShTokens>(x);
@@ -186,6 +182,44 @@ __device__ __forceinline__ float sh_full_stage(uint32_t srow, float scale_log2, 
 // Word w (32 columns) of a 128-bit column mask.
 __device__ __forceinline__ uint32_t sh_word(const uint32_t (&m)[4], int w) {
   return w == 0 ? m[0] : w == 1 ? m[1] : w == 2 ? m[2] : m[3];
+}
+
+// A packed stage with boxes of at most 32 tokens: this row attends only
+// columns of its warp's word, whose 32 scores the caller read.  Their
+// maximum under the mask, the lazy running maximum, then the weights of the
+// word (0 outside the mask, rounded to bf16; the same rounded values enter
+// P.V and the returned row sum) stored at `pword`.  Whole warp.
+__device__ __forceinline__ float sh_word_stage(float (&v)[32], uint32_t bits, float scale_log2,
+                                               float& m_run, float& l_run, float& alpha,
+                                               bool& rescale, int k, uint32_t pword) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = ((bits >> i) & 1u) ? v[i] * scale_log2 : -INFINITY;
+  const float mx = sh_tree_max<32>(v);
+  alpha = 1.f;
+  rescale = false;
+  if (mx > m_run + kShLazyMax) {
+    alpha = fast_exp2(m_run - mx);  // 0 while the row has seen nothing
+    rescale = k > 0;
+    m_run = mx;
+  }
+  l_run *= alpha;
+  // (A row that has attended nothing yet keeps m = -inf: every weight 0.)
+  const float m = m_run == -INFINITY ? 0.f : m_run;
+  uint32_t pw[16];
+  float part[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = q * 8 + 2 * i;
+      pw[q * 4 + i] = pack_bf16x2(fast_exp2(v[t] - m), fast_exp2(v[t + 1] - m));
+      acc += bf16_lo(pw[q * 4 + i]) + bf16_hi(pw[q * 4 + i]);
+    }
+    part[q] = acc;
+  }
+  tc::tmem_st16(pword, pw);
+  return (part[0] + part[1]) + (part[2] + part[3]);
 }
 
 // Pass 1 of a stage: this row's largest score x = s * scale_log2 over the
@@ -541,9 +575,10 @@ __global__ void __launch_bounds__(kShThreads, 1)
     if (!ok) flags[0] = 1;
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // QK of a stage runs at most two stages ahead of its PV (S is
-    // double-buffered); PV waits for the softmax's P (and any rescale of O)
-    // and then releases the stage slot.
+    // QK of stage k waits for its stage's data and for the softmax to have
+    // read S of stage k - 2 (S is double-buffered; the softmax releases it
+    // right after reading it), not for the PV of k - 2; PV waits for the
+    // softmax's P (and any rescale of O) and then releases the stage slot.
     const bool leader = elect_one();
     int next_qk = 0, next_pv = 0;
     bool have_q = n == 0, ok = true;
@@ -581,7 +616,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
           progress = true;
         }
       }
-      if (have_q && next_qk < n && next_qk < next_pv + 2) {
+      if (have_q && next_qk < n && next_qk < next_pv + 4) {
         const int k = next_qk, sb = k & 1, slot = k % NS;
         if (warp_test(full0 + 8u * slot, (k / NS) & 1) &&
             (k < 2 || warp_test(s_free + 8u * sb, ((k >> 1) - 1) & 1))) {
@@ -665,6 +700,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
     }
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    uint32_t p_dirty = 3u;  // bit b: P buffer b may hold weights outside this warp's word
     for (int k = 0; k < n && ok; ++k) {
       const int kg = k_begin + k;
       const int sb = k & 1;
@@ -682,6 +718,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
       const bool shared_stage = kg < n_sh;
       const int nvalid = shared_stage ? min(kShTokens, T - kg * kShTokens) : 0;
       uint32_t mask[4] = {0u, 0u, 0u, 0u};
+      uint32_t myword = 0u;   // packed stage, boxes of up to 32 tokens: word q4's bits
       int my_box_tokens = 0;  // tokens held by the box of token row trow
       if (shared_stage) {
         if (row_ok) sh_mask_set(mask, 0, nvalid);
@@ -698,10 +735,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
             if (row_ok && (e & 0xffff0000) == mine)
               m |= (cnt >= 32 ? 0xffffffffu : ((1u << cnt) - 1u)) << (i * Rb);
           }
-          if (q4 == 0) mask[0] = m;
-          else if (q4 == 1) mask[1] = m;
-          else if (q4 == 2) mask[2] = m;
-          else mask[3] = m;
+          myword = m;
         } else {
           for (int b = 0; b < B; ++b) {
             const int e = meta[slot * kShMaxBoxes + b];
@@ -712,21 +746,61 @@ __global__ void __launch_bounds__(kShThreads, 1)
       if (lane == 0) sh_trace<kTrace>(p, warp, ntr, 43, (uint32_t)k);
       const uint32_t srow = tS + (uint32_t)sb * kShTokens + lane_addr;
       const uint32_t prow = tP + (uint32_t)sb * 64u + lane_addr;
-      // P goes into buffer sb, which the PV of stage k - 2 read.
-      if (k >= 2) {
-        ok = mbar_wait_bounded(pv_done + 8u * sb, ((k >> 1) - 1) & 1, p.err, p.wait_limit);
-        ok = __all_sync(0xffffffffu, ok && !flags[0]);
-        if (!ok) break;
-      }
       float alpha = 1.f;
       bool rescale = false;
       float lw;
-      if (shared_stage && nvalid == kShTokens) {
+      const bool full_stage = shared_stage && nvalid == kShTokens;
+      const bool word_stage = !shared_stage && Rb <= 32;
+      // Scores of a full or a one-word stage are read first and S is
+      // released at once, so the QK two stages on can start while this
+      // stage's weights are computed.  P goes into buffer sb, which the PV of
+      // stage k - 2 read.
+      auto p_buffer_free = [&]() {
+        bool w = true;
+        if (k >= 2) w = mbar_wait_bounded(pv_done + 8u * sb, ((k >> 1) - 1) & 1, p.err,
+                                          p.wait_limit);
+        w = __all_sync(0xffffffffu, w && !flags[0]);
+        tc::fence_after_sync();  // the P stores below come after that P.V
+        return w;
+      };
+      if (full_stage) {
+        float x[kShTokens];
+#pragma unroll
+        for (int c = 0; c < kShTokens / 32; ++c)
+          tc::tmem_ld<32>(srow + (uint32_t)(c * 32), x + 32 * c);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        mbar_arrive(s_free + 8u * sb);
+        if (!(ok = p_buffer_free())) break;
         // A full shared stage: every column, for every row (rows of no
         // member compute weights that are never stored).  The lazy maximum
         // is settled inside, before the weights.
-        lw = sh_full_stage(srow, p.scale_log2, m_run, l_run, alpha, rescale, k, prow);
+        lw = sh_full_stage(x, p.scale_log2, m_run, l_run, alpha, rescale, k, prow);
+        p_dirty |= 1u << sb;
+      } else if (word_stage) {
+        float v[32];
+        tc::tmem_ld<32>(srow + (uint32_t)(q4 * 32), v);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        mbar_arrive(s_free + 8u * sb);
+        if (!(ok = p_buffer_free())) break;
+        lw = sh_word_stage(v, myword, p.scale_log2, m_run, l_run, alpha, rescale, k,
+                           prow + (uint32_t)(q4 * 16));
+        if (p_dirty & (1u << sb)) {
+          // The other words of this buffer still hold an earlier stage's
+          // weights: clear them once (later one-word stages keep them 0).
+          uint32_t z[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            if (w != q4) tc::tmem_st16(prow + (uint32_t)(w * 16), z);
+          p_dirty &= ~(1u << sb);
+        }
       } else {
+        // A shared stage with fewer than 128 tokens, or a packed stage of
+        // boxes wider than 32 tokens: the mask's words, two passes.
+        if (!(ok = p_buffer_free())) break;
         const float mx = sh_stage_max(srow, mask, p.scale_log2);
         // Lazy running maximum: moved only when this stage's scores exceed
         // it by more than kShLazyMax, so weights stay at most 2^kShLazyMax.
@@ -738,6 +812,9 @@ __global__ void __launch_bounds__(kShThreads, 1)
         l_run *= alpha;
         // (A row that has attended nothing yet has m = -inf and weight 0.)
         lw = sh_stage_weights(srow, mask, p.scale_log2, m_run == -INFINITY ? 0.f : m_run, prow);
+        tc::fence_before_sync();
+        mbar_arrive(s_free + 8u * sb);
+        p_dirty |= 1u << sb;
       }
       if (lane == 0) sh_trace<kTrace>(p, warp, ntr, 39, (uint32_t)k);
       if (row_ok) l_run += lw;
@@ -783,7 +860,6 @@ __global__ void __launch_bounds__(kShThreads, 1)
       }
       if (__any_sync(0xffffffffu, stale)) tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      mbar_arrive(s_free + 8u * sb);
       mbar_arrive(p_full + 8u * sb);
       if (lane == 0) sh_trace<kTrace>(p, warp, ntr, 40, (uint32_t)k);
     }

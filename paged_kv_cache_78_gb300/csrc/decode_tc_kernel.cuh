@@ -27,10 +27,11 @@
 //               as soon as each one's inputs are ready;
 //   warps 2..5  softmax warpgroup, one token (QK) or one head dimension (PV)
 //               per tensor-memory lane: online softmax in fp32 (log2 domain),
-//               P^T to shared memory as bf16, each stage's PV tile added into
-//               fp32 registers with the running rescale, and the item's output
-//               (final rows, or a split-KV partial) written at its end.
-// Stage ring slots, S/P/O double buffers and their barriers are indexed by a
+//               P^T to shared memory as bf16; each stage's PV adds into one
+//               fp32 O tile in tensor memory (rescaled there when the running
+//               maximum moves), read once for the item's output (final rows,
+//               or a split-KV partial) at its end.
+// Stage ring slots, S and P double buffers and their barriers are indexed by a
 // stage counter that runs across items, so the pipeline never drains between
 // items.  Every wait is bounded; a timeout records PA_DEVERR_TIMEOUT, the CTA
 // drains its MMAs and TMA loads, frees its tensor memory and returns.  The
