@@ -607,8 +607,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 8, (uint32_t)ii);
         break;
       }
-      if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // next item, fetched early
-      if (it.kind != kItemAttend) continue;
+      if (it.kind != kItemAttend) {
+        if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // the next item
+        continue;
+      }
       // The fused write's rows and target block, loaded now so that their
       // latency overlaps the query load and the first stage's issue; stored
       // before the item's second stage (or its only one) is issued, fenced
@@ -707,6 +709,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
           flags[1] = gk + 1;
           tc_trace<kTrace>(p, 0, ntr, 2, (uint32_t)gk);
+          // The next item's index, fetched once this item's first stage is
+          // on its way (its round trip then overlaps the stages, not the
+          // query load).
+          if (!kBal && k == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
         }
       }
       if (!ok) {
