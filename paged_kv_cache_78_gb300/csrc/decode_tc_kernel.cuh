@@ -421,6 +421,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bg = brange * bq;
       bg_end = min((int)total, bg + bq);
     }
+    // An item's last stage is held back (its boxes resolved, one per lane)
+    // and issued only once the next item is classified, published and its
+    // query load issued: that work then overlaps the wait for the last
+    // stage's slot instead of leaving freed slots idle after it.
+    bool def_have = false, def_fence = false, def_live = false;
+    int def_gk = 0, def_nbox = 0, def_c4 = 0, def_h = 0;
+    auto issue_deferred = [&]() -> bool {
+      if (!def_have) return true;
+      def_have = false;
+      const int slot = def_gk % NS;
+      bool w = true;
+      if (def_gk >= NS) {
+        if (lane == 0)
+          w = mbar_wait_bounded(bars.empty0 + 8u * slot, ((def_gk / NS) - 1) & 1, p.err,
+                                p.wait_limit);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) return false;
+      }
+      if (def_fence) {
+        fence_proxy_async_global();
+        __syncwarp();
+        fence_proxy_async_global();
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bars.full0 + 8u * slot, (uint32_t)def_nbox * box_bytes);
+        tc_trace<kTrace>(p, 0, ntr, 20, (uint32_t)def_gk);
+      }
+      __syncwarp();
+      if (def_live)
+        tma_load_5d(sbase + (uint32_t)slot * (uint32_t)lay.stage + (uint32_t)lane * box_bytes,
+                    &kv_map, bars.full0 + 8u * slot, 0, 0, 0, def_h * kGroups, def_c4);
+      if (lane == 0) {
+        flags[1] = def_gk + 1;
+        tc_trace<kTrace>(p, 0, ntr, 2, (uint32_t)def_gk);
+      }
+      return true;
+    };
     while (true) {
       if (flags[0]) break;
       // Lane 0 classifies the item; the warp follows its decision.
@@ -604,11 +641,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       ++ii;
       if (it.kind == kItemEnd) {
+        if (!issue_deferred()) {
+          flags[0] = 1;
+          break;
+        }
         if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 8, (uint32_t)ii);
         break;
       }
       if (it.kind != kItemAttend) {
         if (!kBal && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);  // the next item
+        if (!issue_deferred()) {
+          flags[0] = 1;
+          break;
+        }
         continue;
       }
       // The fused write's rows and target block, loaded now so that their
@@ -648,6 +693,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         flags[2] = qi;
         tc_trace<kTrace>(p, 0, ntr, 11, (uint32_t)qi);
       }
+      if (!issue_deferred()) {
+        flags[0] = 1;
+        break;
+      }
 
       // The item's K/V stages.  Every lane issues TMA boxes (a box = one
       // block's rows of one 128-byte column group of K or of V): one thread
@@ -655,17 +704,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) tc_trace<kTrace>(p, 0, ntr, 12, (uint32_t)(cur + nxt));
       for (int k = 0; k < it.nstages; ++k, ++gk) {
         const int slot = gk % NS;
-        if (gk >= NS) {
+        const int st_tok = it.tok0 + k * kTcTokens;
+        const int st_n = min(kTcTokens, it.tok1 - st_tok);
+        const int nbox = (st_n + R - 1) >> log2R;
+        const int lb0 = st_tok >> l2bs;
+        // The last stage is held back for the next item's set-up.  Under the
+        // balanced split (pieces of one or two stages are common) only when
+        // its slot is still busy, so that the set-up fills that wait; with
+        // fixed partitions (items of several stages) always.
+        bool defer = k == it.nstages - 1 && nbox <= 32 && gk >= NS;
+        if (kBal && defer) {
+          bool busy = false;
+          if (lane == 0) busy = !mbar_test(bars.empty0 + 8u * slot, ((gk / NS) - 1) & 1);
+          defer = __shfl_sync(0xffffffffu, busy, 0);
+        }
+        if (gk >= NS && !defer) {
           if (lane == 0)
             ok = mbar_wait_bounded(bars.empty0 + 8u * slot, ((gk / NS) - 1) & 1, p.err,
                                    p.wait_limit);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
-        const int st_tok = it.tok0 + k * kTcTokens;
-        const int st_n = min(kTcTokens, it.tok1 - st_tok);
-        const int nbox = (st_n + R - 1) >> log2R;
-        const int lb0 = st_tok >> l2bs;
         while (lb0 >= win + 32) {
           cur = nxt;
           win += 32;
@@ -674,6 +733,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (k == k_store)
           store_new_token(p.cache_w, new_kv, new_id, it.h, it.tok1 - 1, p.num_kv_heads, D * 2 / 16,
                           BS, p.num_blocks, p.err, lane);
+        if (defer) {
+          // Resolve the last stage's boxes now (this item's table window is
+          // replaced by the next item's) and issue them later.
+          const bool live = lane < nbox;
+          const int tk = st_tok + ((live ? lane : 0) << log2R);
+          const int src = (tk >> l2bs) - win;  // 0 .. 47
+          const int id_cur = __shfl_sync(0xffffffffu, cur, src & 31);
+          const int id_nxt = __shfl_sync(0xffffffffu, nxt, src & 31);
+          const int id = src < 32 ? id_cur : id_nxt;
+          int c4 = id * chunks_per_block + ((tk & (BS - 1)) >> 3);
+          if (live && (id < 0 || id >= p.num_blocks)) {
+            record_error(p.err, PA_DEVERR_BLOCK_ID);
+            c4 = p.num_blocks * chunks_per_block;  // outside the tensor: zero fill
+          }
+          def_have = true;
+          def_live = live;
+          def_c4 = c4;
+          def_gk = gk;
+          def_nbox = nbox;
+          def_h = it.h;
+          def_fence = k == k_fence;
+          if (!kBal && k == 0 && lane == 0) idx = gridDim.x + atomicAdd(p.sched, 1u);
+          continue;
+        }
         if (k == k_fence) {
           // The newest token lands in this stage: its store is ordered before
           // the stage's TMA reads.
