@@ -560,8 +560,9 @@ const char* pa_status_string(pa_status status);
  * record 2 * SMs on: producer 30 start (global timer, ns), 31 prologue done
  * (its stages), 32 stage slot free (stage), 33 stage's boxes issued, 34 next
  * stage's blocks resolved; MMA issuer 35 QK issued (stage), 36 PV issued
- * (stage); softmax warps 2..5: 37 query rows stored, 38 scores ready
- * (stage), 43 stage's masks built (stage), 39 stage's weights written to
+ * (stage); softmax warps 2..5: 37 query rows stored, 38 stage's data
+ * landed (stage), 43 masks built and scores ready (stage), 39 stage's
+ * weights written to
  * tensor memory (stage), 46 O rescale stores issued (stage), 47 O rescale
  * stores done (stage), 40 P published (stage), 42 last P.V done, 41 rows or
  * partials written.

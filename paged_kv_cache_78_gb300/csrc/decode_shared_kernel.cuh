@@ -705,12 +705,12 @@ __global__ void __launch_bounds__(kShThreads, 1)
       const int kg = k_begin + k;
       const int sb = k & 1;
       const int slot = k % NS;
-      ok = mbar_wait_bounded(s_full + 8u * sb, (k >> 1) & 1, p.err, p.wait_limit) &&
-           mbar_wait_bounded(full0 + 8u * slot, (k / NS) & 1, p.err, p.wait_limit);
+      // The stage's box table is readable once its data has landed, which
+      // is before its scores are: the masks are built while QK runs.
+      ok = mbar_wait_bounded(full0 + 8u * slot, (k / NS) & 1, p.err, p.wait_limit);
       ok = __all_sync(0xffffffffu, ok && !flags[0]);
       if (!ok) break;
       if (lane == 0) sh_trace<kTrace>(p, warp, ntr, 38, (uint32_t)k);
-      tc::fence_after_sync();
       // Columns this row attends: a shared stage's tokens below T, or the
       // boxes of this row's member (for boxes of up to 32 tokens only this
       // warp's word can hold them).  A token row of the stage is stale (its
@@ -743,6 +743,10 @@ __global__ void __launch_bounds__(kShThreads, 1)
           }
         }
       }
+      ok = mbar_wait_bounded(s_full + 8u * sb, (k >> 1) & 1, p.err, p.wait_limit);
+      ok = __all_sync(0xffffffffu, ok && !flags[0]);
+      if (!ok) break;
+      tc::fence_after_sync();
       if (lane == 0) sh_trace<kTrace>(p, warp, ntr, 43, (uint32_t)k);
       const uint32_t srow = tS + (uint32_t)sb * kShTokens + lane_addr;
       const uint32_t prow = tP + (uint32_t)sb * 64u + lane_addr;
